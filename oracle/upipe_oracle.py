@@ -1,0 +1,496 @@
+"""fp64 oracle of the UPipe headwise-chunked causal GQA self-attention layer.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()``
+and ``bench.py``'s cpu baseline / reference arm may import or run this
+module.  The CUDA library never calls it, and it imports nothing from the
+library: the two share no code.  Inputs arrive as float64 arrays upcast
+exactly from the bf16 bits made by ``synthetic``.
+
+Plain and slow on purpose: materialised score matrices, one head at a time,
+numpy matmul as the only library primitive.
+
+Sources (page title and section):
+
+[U1] "Untied Ulysses: Memory-Efficient Context Parallelism via Headwise
+     Chunking", summary page (paper.rainbus.top):
+       - Background / DeepSpeed Ulysses: an all-to-all turns S/C-token
+         sequence shards into all-token head shards and back.
+       - Background / GQA: H query heads share G key/value heads, each KV
+         head serving H/G query heads.
+       - Motivation: Ulysses attention memory 12*(S/C)*H*d_head bytes.
+       - Core method: H/U stages of U heads; buffers reused across stages;
+         at U = C the peak is 12*S*d_head; Qwen3-32B (H=64, C=8) 96 vs 12.
+       - Method steps (1)-(4): project X onto heads iU..(i+1)U-1 (QKV
+         6*(S/C)*U*d_head bytes), all-to-all to U/C heads per rank (buffer
+         6*(S/C)*U*d_head), attention, all-to-all back.
+       - Novelty: GQA schedule processes heads out of order so every unique
+         KV head is communicated in the first stage and later stages move
+         query heads only.
+       - Limitations: U must be divisible by C.
+[U3] Same title, arXiv abstract (fugumt.com): chunking at the attention
+     head level; up to 87.5% less intermediate memory for 32B models.
+
+Readings where the pages are silent or garbled (each listed in the design doc):
+  * attention is softmax(Q K^T / sqrt(d_head) + causal mask) V with key j
+    visible to query i iff j <= i; no bias, positional rotation or dropout;
+  * query head h uses KV head h // (H/G) (contiguous groups);
+  * in-order stage i holds heads iU..(i+1)U-1, rank r the r-th block of U/C;
+    every query slot receives its own copy of its KV head, which is what
+    makes the QKV exchange buffer exactly 6*(S/C)*U*d_head bytes;
+  * out-of-order: rank r owns query heads r*H/C..(r+1)*H/C-1 over all
+    stages, U/C of them per stage; the KV heads those use move once, in
+    stage 0, and stay resident;
+  * each stage adds its heads' share O_s W_o[rows of s] to Y;
+  * the backward pass (absent from the pages) is the analytic gradient of
+    L = <Y, dY>; only O and the log-sum-exp are kept from the forward pass.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+IN_ORDER = 0
+GQA_OUT_OF_ORDER = 1
+
+
+# ---------------------------------------------------------------------------
+# shapes, head grouping and schedules
+# ---------------------------------------------------------------------------
+
+def kv_head(h: int, H: int, G: int) -> int:
+    """[U1] Background/GQA: each run of H/G consecutive query heads shares one KV head."""
+    return h // (H // G)
+
+
+def check_shape(S, d_model, H, G, d_head, U, C, order=IN_ORDER):
+    """Divisibility the method needs: [U1] Limitations (C | U), Method steps
+    (H/U stages of U heads, S/C tokens per rank), Background/GQA (G | H)."""
+    if min(S, d_model, H, G, d_head, U, C) <= 0:
+        raise ValueError("all sizes must be positive")
+    if H % U:
+        raise ValueError("U must divide H")
+    if U % C:
+        raise ValueError("C must divide U")
+    if S % C:
+        raise ValueError("C must divide S")
+    if H % G:
+        raise ValueError("G must divide H")
+    if order == GQA_OUT_OF_ORDER and not (G % C == 0 or C % G == 0):
+        raise ValueError("out-of-order schedule needs C | G or G | C")
+
+
+def stage_heads(H: int, G: int, U: int, C: int, order: int = IN_ORDER) -> np.ndarray:
+    """Query head held by (stage i, rank r, slot j): array [H/U, C, U/C].
+
+    In order ([U1] Method steps (1)-(2)): stage i covers heads iU..(i+1)U-1
+    and rank r receives the r-th run of U/C of them.
+    Out of order ([U1] Novelty): rank r keeps the query heads of one block of
+    H/C heads for every stage and works through them U/C at a time, so the KV
+    heads it needs never change after stage 0.
+    """
+    n_stages, per_rank = H // U, U // C
+    out = np.empty((n_stages, C, per_rank), dtype=np.int64)
+    for i in range(n_stages):
+        for r in range(C):
+            for j in range(per_rank):
+                if order == IN_ORDER:
+                    out[i, r, j] = i * U + r * per_rank + j
+                else:
+                    out[i, r, j] = r * (H // C) + i * per_rank + j
+    return out
+
+
+def rank_kv_heads(H: int, G: int, U: int, C: int, r: int, order: int) -> list:
+    """KV heads rank r holds resident under the out-of-order schedule: the set
+    of KV heads its query heads use, over all stages ([U1] Novelty)."""
+    sched = stage_heads(H, G, U, C, order)
+    return sorted({kv_head(int(h), H, G) for h in sched[:, r, :].ravel()})
+
+
+def kv_moves(H, G, U, C, order):
+    """(stage, rank, kv head) triples for every KV head sent to a rank.
+
+    In order, every query slot receives the KV head it uses, in every stage.
+    Out of order, rank r receives its resident KV heads once, in stage 0.
+    """
+    sched = stage_heads(H, G, U, C, order)
+    moves = []
+    for i in range(H // U):
+        for r in range(C):
+            if order == IN_ORDER:
+                for j in range(U // C):
+                    moves.append((i, r, kv_head(int(sched[i, r, j]), H, G)))
+            elif i == 0:
+                for g in rank_kv_heads(H, G, U, C, r, order):
+                    moves.append((0, r, g))
+    return moves
+
+
+# ---------------------------------------------------------------------------
+# memory closed forms ([U1] Motivation, Core method, Method steps)
+# ---------------------------------------------------------------------------
+
+def ulysses_attention_bytes_per_rank(S, C, H, d_head):
+    """[U1] Motivation: Ulysses keeps QKV and the all-to-all buffers of all H
+    heads: 12*(S/C)*H*d_head bytes per device (16-bit elements)."""
+    return 12 * (S // C) * H * d_head
+
+
+def upipe_stage_bytes_per_rank(S, C, U, d_head):
+    """[U1] Method steps (1)+(2): projected QKV 6*(S/C)*U*d_head bytes plus the
+    exchange buffer of the same size; reused by every stage."""
+    qkv = 6 * (S // C) * U * d_head
+    exchange = 6 * (S // C) * U * d_head
+    return qkv + exchange
+
+
+def upipe_output_bytes_per_rank(S, C, U, d_head):
+    """[U1] Method steps (3)+(4), with the printed d_model read as d_head (an
+    output of U heads has U*d_head values per token): 2*(S/C)*U*d_head for the
+    attention output and the same for its exchange buffer."""
+    return 2 * (S // C) * U * d_head + 2 * (S // C) * U * d_head
+
+
+# ---------------------------------------------------------------------------
+# attention core (one query head against its KV head)
+# ---------------------------------------------------------------------------
+
+def causal_scores(q, k):
+    """A = q k^T / sqrt(d_head) with -inf where key j comes after query i."""
+    d = q.shape[1]
+    A = (q @ k.T) / np.sqrt(d)
+    n = q.shape[0]
+    A[np.triu_indices(n, k=1)] = -np.inf
+    return A
+
+
+def attention_head_forward(q, k, v):
+    """O = softmax(A) v per row; lse_i = ln sum_{j<=i} exp(A_ij).  Returns (O, lse, P)."""
+    A = causal_scores(q, k)
+    m = A.max(axis=1, keepdims=True)
+    E = np.exp(A - m)
+    l = E.sum(axis=1, keepdims=True)
+    P = E / l
+    return P @ v, (m + np.log(l))[:, 0], P
+
+
+def attention_head_backward(q, k, v, P, o, do):
+    """Analytic gradients of <O, dO> for one head: (dq, dk, dv).
+
+    dv = P^T dO;  dP = dO v^T;  dA = P * (dP - rowsum(dO * O));
+    dq = dA k / sqrt(d);  dk = dA^T q / sqrt(d).
+    """
+    d = q.shape[1]
+    dv = P.T @ do
+    dP = do @ v.T
+    D = (do * o).sum(axis=1, keepdims=True)
+    dA = P * (dP - D)
+    dq = dA @ k / np.sqrt(d)
+    dk = dA.T @ q / np.sqrt(d)
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# the layer, all heads at once (the definition)
+# ---------------------------------------------------------------------------
+
+def split_w_qkv(W_qkv, H, G, d_head):
+    """W_qkv [d_model, (H+2G)*d_head] -> per-head column blocks (Wq[h], Wk[g], Wv[g])."""
+    d = d_head
+    Wq = [W_qkv[:, h * d:(h + 1) * d] for h in range(H)]
+    Wk = [W_qkv[:, (H + g) * d:(H + g + 1) * d] for g in range(G)]
+    Wv = [W_qkv[:, (H + G + g) * d:(H + G + g + 1) * d] for g in range(G)]
+    return Wq, Wk, Wv
+
+
+def layer_forward(X, W_qkv, W_o, H, G, d_head):
+    """Y = [O_0 ... O_{H-1}] W_o with O_h = causal attention of head h.
+
+    Returns (Y [S, d_model], O [S, H*d_head], lse [H, S]).
+    """
+    S = X.shape[0]
+    d = d_head
+    Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
+    K = [X @ Wk[g] for g in range(G)]
+    V = [X @ Wv[g] for g in range(G)]
+    O = np.zeros((S, H * d))
+    lse = np.zeros((H, S))
+    for h in range(H):
+        g = kv_head(h, H, G)
+        o, l, _ = attention_head_forward(X @ Wq[h], K[g], V[g])
+        O[:, h * d:(h + 1) * d] = o
+        lse[h] = l
+    return O @ W_o, O, lse
+
+
+def layer_backward(X, W_qkv, W_o, H, G, d_head, dY):
+    """Gradients of L = <Y, dY>: returns (dX, dW_qkv, dW_o)."""
+    S, d_model = X.shape
+    d = d_head
+    Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
+    K = [X @ Wk[g] for g in range(G)]
+    V = [X @ Wv[g] for g in range(G)]
+    dK = [np.zeros((S, d)) for _ in range(G)]
+    dV = [np.zeros((S, d)) for _ in range(G)]
+    O = np.zeros((S, H * d))
+    dW_qkv = np.zeros_like(W_qkv)
+    dX = np.zeros_like(X)
+    for h in range(H):
+        g = kv_head(h, H, G)
+        q = X @ Wq[h]
+        o, _, P = attention_head_forward(q, K[g], V[g])
+        O[:, h * d:(h + 1) * d] = o
+        do = dY @ W_o[h * d:(h + 1) * d, :].T
+        dq, dk, dv = attention_head_backward(q, K[g], V[g], P, o, do)
+        dK[g] += dk
+        dV[g] += dv
+        dW_qkv[:, h * d:(h + 1) * d] = X.T @ dq
+        dX += dq @ Wq[h].T
+    for g in range(G):
+        dW_qkv[:, (H + g) * d:(H + g + 1) * d] = X.T @ dK[g]
+        dW_qkv[:, (H + G + g) * d:(H + G + g + 1) * d] = X.T @ dV[g]
+        dX += dK[g] @ Wk[g].T + dV[g] @ Wv[g].T
+    dW_o = O.T @ dY
+    return dX, dW_qkv, dW_o
+
+
+def layer_forward_rows(X, W_qkv, W_o, H, G, d_head, rows):
+    """Y at the given query positions only (exact: each row needs keys 0..row)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    d = d_head
+    n = int(rows.max()) + 1
+    Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
+    Xp = X[:n]
+    K = [Xp @ Wk[g] for g in range(G)]
+    V = [Xp @ Wv[g] for g in range(G)]
+    O = np.zeros((len(rows), H * d))
+    lse = np.zeros((H, len(rows)))
+    for h in range(H):
+        g = kv_head(h, H, G)
+        q = X[rows] @ Wq[h]
+        for t, i in enumerate(rows):
+            a = (K[g][:i + 1] @ q[t]) / np.sqrt(d)
+            m = a.max()
+            e = np.exp(a - m)
+            O[t, h * d:(h + 1) * d] = (e @ V[g][:i + 1]) / e.sum()
+            lse[h, t] = m + np.log(e.sum())
+    return O @ W_o, O, lse
+
+
+# ---------------------------------------------------------------------------
+# the all-to-all on C virtual ranks
+# ---------------------------------------------------------------------------
+
+def all_to_all(send):
+    """send[c][r] is what rank c sends to rank r; returns recv with recv[r][c] = send[c][r]."""
+    C = len(send)
+    return [[send[c][r] for c in range(C)] for r in range(C)]
+
+
+def seq_to_head(shards, wanted):
+    """Ulysses input exchange ([U1] Background, Method steps (2)).
+
+    shards[c]: dict head -> [S/C, d] block rank c computed for its tokens.
+    wanted[r]: list of heads rank r must hold after the exchange.
+    Returns per rank r an array [len(wanted[r]), S, d]: every wanted head over
+    all S tokens, token blocks in rank order.
+    """
+    C = len(shards)
+    send = [[np.stack([shards[c][h] for h in wanted[r]]) if wanted[r] else None
+             for r in range(C)] for c in range(C)]
+    recv = all_to_all(send)
+    return [np.concatenate(recv[r], axis=1) if wanted[r] else None for r in range(C)]
+
+
+def head_to_seq(held, heads_of, S):
+    """Ulysses output exchange ([U1] Method steps (4)).
+
+    held[r]: array [n_r, S, d] of the heads heads_of[r] on rank r.
+    Returns per rank c a list of (head, [S/C, d] block) pairs, in the order the
+    ranks send them (ascending source rank, then slot).
+    """
+    C = len(held)
+    Sc = S // C
+    send = [[[(h, held[r][j, c * Sc:(c + 1) * Sc]) for j, h in enumerate(heads_of[r])]
+             for c in range(C)] for r in range(C)]
+    recv = all_to_all(send)
+    return [[pair for blocks in recv[c] for pair in blocks] for c in range(C)]
+
+
+# ---------------------------------------------------------------------------
+# the staged layer: H/U stages on C virtual ranks ([U1] Method steps)
+# ---------------------------------------------------------------------------
+
+def _stage_kv_wanted(sched_i, H, G, C, order, stage, resident):
+    """KV heads each rank receives in this stage (one per query slot in order;
+    the resident set in stage 0 only, out of order)."""
+    if order == IN_ORDER:
+        return [[kv_head(int(h), H, G) for h in sched_i[r]] for r in range(C)]
+    return [list(resident[r]) if stage == 0 else [] for r in range(C)]
+
+
+def staged_forward(X, W_qkv, W_o, H, G, d_head, U, C, order=IN_ORDER):
+    """The layer run as H/U stages of U heads on C virtual ranks.
+
+    Stage i: (1) each rank projects its S/C tokens onto the stage's heads;
+    (2) all-to-all to head shards; (3) causal attention per held head;
+    (4) all-to-all of the outputs back to sequence shards; then each rank adds
+    the stage's heads' share of the output projection to its Y shard.
+    Returns (Y, O [S, H*d], lse [H, S]) like ``layer_forward``.
+    """
+    S, d_model = X.shape
+    check_shape(S, d_model, H, G, d_head, U, C, order)
+    d, Sc = d_head, S // C
+    Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
+    sched = stage_heads(H, G, U, C, order)
+    resident = [rank_kv_heads(H, G, U, C, r, order) for r in range(C)] \
+        if order == GQA_OUT_OF_ORDER else None
+    Xs = [X[c * Sc:(c + 1) * Sc] for c in range(C)]
+    Y = [np.zeros((Sc, d_model)) for _ in range(C)]
+    O_saved = np.zeros((S, H * d))
+    lse = np.zeros((H, S))
+    K_held = V_held = None
+    for i in range(H // U):
+        q_wanted = [list(map(int, sched[i, r])) for r in range(C)]
+        kv_wanted = _stage_kv_wanted(sched[i], H, G, C, order, i, resident)
+        kv_needed = sorted({g for r in range(C) for g in kv_wanted[r]})
+        # (1) projection on every rank's sequence shard
+        Qs = [{h: Xs[c] @ Wq[h] for r in range(C) for h in q_wanted[r]} for c in range(C)]
+        Ks = [{g: Xs[c] @ Wk[g] for g in kv_needed} for c in range(C)]
+        Vs = [{g: Xs[c] @ Wv[g] for g in kv_needed} for c in range(C)]
+        # (2) exchange to head shards
+        Q_held = seq_to_head(Qs, q_wanted)
+        if kv_needed:
+            K_new, V_new = seq_to_head(Ks, kv_wanted), seq_to_head(Vs, kv_wanted)
+            K_held = [(kv_wanted[r], K_new[r]) for r in range(C)]
+            V_held = [(kv_wanted[r], V_new[r]) for r in range(C)]
+        # (3) attention on each rank's heads
+        O_held = []
+        for r in range(C):
+            outs = []
+            for j, h in enumerate(q_wanted[r]):
+                g = kv_head(h, H, G)
+                slot = j if order == IN_ORDER else K_held[r][0].index(g)
+                o, l, _ = attention_head_forward(Q_held[r][j], K_held[r][1][slot],
+                                                 V_held[r][1][slot])
+                outs.append(o)
+                lse[h] = l
+            O_held.append(np.stack(outs))
+        # (4) exchange back, then the stage's share of the output projection
+        O_back = head_to_seq(O_held, q_wanted, S)
+        for c in range(C):
+            for h, blk in O_back[c]:
+                O_saved[c * Sc:(c + 1) * Sc, h * d:(h + 1) * d] = blk
+                Y[c] += blk @ W_o[h * d:(h + 1) * d, :]
+    return np.concatenate(Y), O_saved, lse
+
+
+def staged_backward(X, W_qkv, W_o, H, G, d_head, U, C, dY, O_saved, lse, order=IN_ORDER):
+    """Backward of the staged layer, stage by stage.
+
+    Per stage: recompute (1)+(2) for the stage's heads; dO = dY W_o[rows]^T on
+    each sequence shard, exchanged to head shards with the saved O; attention
+    backward from the saved lse; the exchange back of dQ (and of dK, dV, whose
+    per-slot copies are summed per KV head); then each rank adds its shard's
+    share to dX and to the weight gradients.  Out of order, dK and dV stay on
+    their resident ranks and go back once, after the last stage.
+    Returns (dX, dW_qkv, dW_o).
+    """
+    S, d_model = X.shape
+    check_shape(S, d_model, H, G, d_head, U, C, order)
+    d, Sc = d_head, S // C
+    Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
+    sched = stage_heads(H, G, U, C, order)
+    resident = [rank_kv_heads(H, G, U, C, r, order) for r in range(C)] \
+        if order == GQA_OUT_OF_ORDER else None
+    Xs = [X[c * Sc:(c + 1) * Sc] for c in range(C)]
+    dYs = [dY[c * Sc:(c + 1) * Sc] for c in range(C)]
+    Os = [O_saved[c * Sc:(c + 1) * Sc] for c in range(C)]
+    dX = [np.zeros((Sc, d_model)) for _ in range(C)]
+    dW_qkv = np.zeros_like(W_qkv)
+    dK_res = dV_res = None
+    K_held = V_held = None
+    for i in range(H // U):
+        q_wanted = [list(map(int, sched[i, r])) for r in range(C)]
+        kv_wanted = _stage_kv_wanted(sched[i], H, G, C, order, i, resident)
+        kv_needed = sorted({g for r in range(C) for g in kv_wanted[r]})
+        Qs = [{h: Xs[c] @ Wq[h] for r in range(C) for h in q_wanted[r]} for c in range(C)]
+        Ks = [{g: Xs[c] @ Wk[g] for g in kv_needed} for c in range(C)]
+        Vs = [{g: Xs[c] @ Wv[g] for g in kv_needed} for c in range(C)]
+        dOs = [{h: dYs[c] @ W_o[h * d:(h + 1) * d, :].T for r in range(C) for h in q_wanted[r]}
+               for c in range(C)]
+        Osv = [{h: Os[c][:, h * d:(h + 1) * d] for r in range(C) for h in q_wanted[r]}
+               for c in range(C)]
+        Q_held = seq_to_head(Qs, q_wanted)
+        dO_held = seq_to_head(dOs, q_wanted)
+        O_held = seq_to_head(Osv, q_wanted)
+        if kv_needed:
+            K_new, V_new = seq_to_head(Ks, kv_wanted), seq_to_head(Vs, kv_wanted)
+            K_held = [(kv_wanted[r], K_new[r]) for r in range(C)]
+            V_held = [(kv_wanted[r], V_new[r]) for r in range(C)]
+            if order == GQA_OUT_OF_ORDER:
+                dK_res = [np.zeros_like(K_new[r]) for r in range(C)]
+                dV_res = [np.zeros_like(V_new[r]) for r in range(C)]
+        dQ_held, dK_slot, dV_slot = [], [], []
+        for r in range(C):
+            dq_r, dk_r, dv_r = [], [], []
+            for j, h in enumerate(q_wanted[r]):
+                g = kv_head(h, H, G)
+                slot = j if order == IN_ORDER else K_held[r][0].index(g)
+                k, v = K_held[r][1][slot], V_held[r][1][slot]
+                q, o, do = Q_held[r][j], O_held[r][j], dO_held[r][j]
+                # P rebuilt from the saved log-sum-exp
+                P = np.exp(causal_scores(q, k) - lse[h][:, None])
+                dq, dk, dv = attention_head_backward(q, k, v, P, o, do)
+                dq_r.append(dq)
+                if order == IN_ORDER:
+                    dk_r.append(dk)
+                    dv_r.append(dv)
+                else:
+                    dK_res[r][slot] += dk
+                    dV_res[r][slot] += dv
+            dQ_held.append(np.stack(dq_r))
+            if order == IN_ORDER:
+                dK_slot.append(np.stack(dk_r))
+                dV_slot.append(np.stack(dv_r))
+        dQ_back = head_to_seq(dQ_held, q_wanted, S)
+        for c in range(C):
+            for h, blk in dQ_back[c]:
+                dX[c] += blk @ Wq[h].T
+                dW_qkv[:, h * d:(h + 1) * d] += Xs[c].T @ blk
+        if order == IN_ORDER:
+            _kv_back_and_project(dK_slot, dV_slot, kv_wanted, Xs, Wk, Wv, dX, dW_qkv, H, G, d, S)
+    if order == GQA_OUT_OF_ORDER:
+        _kv_back_and_project(dK_res, dV_res, resident, Xs, Wk, Wv, dX, dW_qkv, H, G, d, S)
+    dW_o = sum(Os[c].T @ dYs[c] for c in range(C))
+    return np.concatenate(dX), dW_qkv, dW_o
+
+
+def _kv_back_and_project(dK_held, dV_held, heads_of, Xs, Wk, Wv, dX, dW_qkv, H, G, d, S):
+    """Exchange dK, dV back to sequence shards, sum the copies of each KV head
+    (ascending source rank, then slot), and add their projection gradients."""
+    C = len(Xs)
+    dK_back = head_to_seq(dK_held, heads_of, S)
+    dV_back = head_to_seq(dV_held, heads_of, S)
+    for c in range(C):
+        dk_sum, dv_sum = {}, {}
+        for (g, blk) in dK_back[c]:
+            dk_sum[g] = dk_sum.get(g, 0.0) + blk
+        for (g, blk) in dV_back[c]:
+            dv_sum[g] = dv_sum.get(g, 0.0) + blk
+        for g in dk_sum:
+            dX[c] += dk_sum[g] @ Wk[g].T + dv_sum[g] @ Wv[g].T
+            dW_qkv[:, (H + g) * d:(H + g + 1) * d] += Xs[c].T @ dk_sum[g]
+            dW_qkv[:, (H + G + g) * d:(H + G + g + 1) * d] += Xs[c].T @ dv_sum[g]
+
+
+# ---------------------------------------------------------------------------
+# FLOP accounting (model FLOPs; not a method step)
+# ---------------------------------------------------------------------------
+
+def layer_model_flops(S, d_model, H, G, d_head):
+    """Forward model FLOPs of the layer: projections plus causal attention
+    (half of the dense QK^T and PV); fwd+bwd counts 3x this."""
+    proj = 2 * S * d_model * (H + 2 * G) * d_head
+    out = 2 * S * H * d_head * d_model
+    attn = 2 * S * S * H * d_head  # (2 matmuls x 2 flops x S^2/2)
+    return proj + out + attn
