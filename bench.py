@@ -1,0 +1,365 @@
+#!/usr/bin/env python3
+"""Benchmark of the headwise-chunked (UPipe) causal GQA attention layer, fwd+bwd.
+
+One step = one forward and one backward pass of the whole layer (every stage:
+projection, exchange, attention, exchange back, output projection, and the
+matching backward work) over one synthetic batch.  Default workload: the
+Llama3-8B-shaped layer, S=32768, d_model=4096, H=32, G=8, d_head=128, U=8,
+C=8 virtual ranks, bf16 in / fp32 accumulate.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+instead (the only other code path allowed to run it), on a bounded sample.
+Under torchrun with N > 1 every rank runs an independent replica on its own
+GPU (the layer does not shard across GPUs here); value = tokens over all
+ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn-layer fwd+bwd tokens/s & TFLOP/s (% BF16 peak) at 1 GB300; peak bytes vs U"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "llama3_8b_32k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.th = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                self.rows.append(f)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.th:
+            self.th.join(timeout=2)
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in self.rows if num(r[1])]
+        mx = [num(r[2]) for r in self.rows if num(r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        load = [s for s in sm if mx and s > 0.3 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def model_flops_step(sh):
+    """Model FLOPs of one fwd+bwd step: 3x the forward, which is the QKV
+    projection, the output projection and causal attention (QK^T and PV over
+    the S(S+1)/2 visible pairs).  Recomputation is not counted."""
+    S, dm, H, G, d = sh.S, sh.d_model, sh.H, sh.G, sh.d_head
+    fwd = 2 * S * dm * (H + 2 * G) * d + 2 * S * H * d * dm + 2 * 2 * d * H * S * (S + 1) / 2
+    return 3 * fwd
+
+
+def oracle_sample(sh, S_sample, seed=0):
+    """Time the fp64 oracle (fwd+bwd) on the workload's widths at S_sample tokens.
+    Returns (seconds, tokens/s extrapolated to the workload by model-FLOP ratio)."""
+    import numpy as np
+    from oracle import upipe_oracle as orc
+    from synthetic import layer_inputs, bf16_bits_to_f64
+    small = sh.replace(S=S_sample, U=sh.U, C=sh.C)
+    bits = layer_inputs(small, seed)
+    X, Wqkv, Wo, dY = (bf16_bits_to_f64(bits[k]) for k in ("X", "W_qkv", "W_o", "dY"))
+    t0 = time.perf_counter()
+    orc.layer_forward(X, Wqkv, Wo, small.H, small.G, small.d_head)
+    orc.layer_backward(X, Wqkv, Wo, small.H, small.G, small.d_head, dY)
+    dt = time.perf_counter() - t0
+    ratio = model_flops_step(sh) / model_flops_step(small)
+    return dt, sh.S / (dt * ratio)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, sh):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    S_sample = args.ref_sample_tokens
+    for _ in range(args.warmup):
+        oracle_sample(sh, S_sample)
+    times, vals = [], []
+    for _ in range(args.steps):
+        dt, v = oracle_sample(sh, S_sample)
+        times.append(dt)
+        vals.append(v)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": statistics.median(times) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args, sh),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"fp64 numpy oracle fwd+bwd at the workload's widths with S={S_sample} "
+                                   f"per step, tokens/s extrapolated to S={sh.S} by the model-FLOP ratio"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(args, sh):
+    return {"workload": args.workload, "S": sh.S, "d_model": sh.d_model, "H": sh.H, "G": sh.G,
+            "d_head": sh.d_head, "U": sh.U, "C": sh.C, "schedule": "gqa_out_of_order" if args.sched else "in_order",
+            "causal": True, "l2": "inputs larger than L2 (X and dY are 2*S*d_model bf16 each; every step streams "
+                                  "GBs through HBM)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--sched", type=int, default=0, help="0 in order, 1 GQA out of order")
+    ap.add_argument("--U", type=int, default=None, help="override heads per stage")
+    ap.add_argument("--S", type=int, default=None, help="override sequence length")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
+    ap.add_argument("--ref-sample-tokens", type=int, default=2048)
+    args = ap.parse_args()
+
+    from synthetic import SHAPES
+    sh = SHAPES[args.workload]
+    if args.U:
+        sh = sh.replace(U=args.U)
+    if args.S:
+        sh = sh.replace(S=args.S)
+    if args.impl == "reference":
+        return run_reference(args, sh)
+
+    rank, world, local = dist_env()
+    import numpy as np
+    import torch
+    import headwise_chunked_ulysses_gb300 as upipe
+    from synthetic import layer_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    s = upipe.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, sh.U, sh.C, args.sched)
+    bits = layer_inputs(sh, seed=0)
+    host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) for k, v in bits.items()}
+    d = {k: v.to(dev) for k, v in host.items()}
+    bf, f32 = torch.bfloat16, torch.float32
+    Y = torch.empty(sh.S, sh.d_model, dtype=bf, device=dev)
+    O = torch.empty(sh.S, sh.H * sh.d_head, dtype=bf, device=dev)
+    lse = torch.empty(sh.H, sh.S, dtype=f32, device=dev)
+    dX = torch.empty(sh.S, sh.d_model, dtype=bf, device=dev)
+    dWqkv = torch.empty(sh.d_model, sh.qkv_cols, dtype=f32, device=dev)
+    dWo = torch.empty(sh.H * sh.d_head, sh.d_model, dtype=f32, device=dev)
+    wsf = torch.empty(upipe.fwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(upipe.bwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        _, _, _, stf = upipe.attn_fwd(d["X"], d["W_qkv"], d["W_o"], s, Y=Y, O_saved=O, lse=lse, ws=wsf)
+        _, _, _, stb = upipe.attn_bwd(d["X"], d["W_qkv"], d["W_o"], O, lse, d["dY"], s, dX=dX, dW_qkv=dWqkv,
+                                      dW_o=dWo, ws=wsb)
+        return stf, stb
+
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem_before = torch.cuda.memory_allocated(dev)
+    for _ in range(args.warmup):
+        stf, stb = step()
+    barrier()
+    upipe.sync_status()
+
+    # ---------------- device-resident timed region ----------------
+    clocks = ClockSampler(local)
+    clocks.start()
+    upipe.profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        stf, stb = step()
+    e1.record(stream)
+    barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    prof = upipe.profile_read()
+    upipe.profile_enable(False)
+    clk = clocks.stop()
+    upipe.sync_status()
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_step = elapsed_ms / args.steps
+    tokens_per_s = world * sh.S * args.steps / (elapsed_ms / 1e3)
+    pk = peaks()
+    flops_step = model_flops_step(sh)
+    tflops = flops_step / (ms_step / 1e3) / 1e12
+    peak_tf = pk["bf16_tflops_sustained"]
+
+    # per-kernel achieved throughput from the live event timings
+    kernels = {}
+    for k in upipe.KERNEL_KINDS:
+        ms, n = prof[k]
+        n_step = stf["launches_by_kind"][k] + stb["launches_by_kind"][k]
+        fl = (stf["flops_by_kind"][k] + stb["flops_by_kind"][k]) * args.steps
+        by = (stf["bytes_by_kind"][k] + stb["bytes_by_kind"][k]) * args.steps
+        kernels[k] = {"ms_per_step": ms / args.steps, "launches_per_step": n_step, "share": None,
+                      "tflops": fl / (ms / 1e3) / 1e12 if ms > 0 and fl > 0 else None,
+                      "gbs": by / (ms / 1e3) / 1e9 if ms > 0 else None}
+    tot = sum(v["ms_per_step"] for v in kernels.values()) or 1.0
+    for v in kernels.values():
+        v["share"] = v["ms_per_step"] / tot
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
+    ms_dom, n_dom = prof[dom]
+    if kernels[dom]["tflops"]:
+        fl_launch = (stf["flops_by_kind"][dom] + stb["flops_by_kind"][dom]) / max(1, kernels[dom]["launches_per_step"])
+        achieved = fl_launch / (ms_dom / n_dom / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf, "peak_source": f"{pk['source']} bf16_tflops_sustained",
+                "flops_per_launch": fl_launch, "ms_per_launch": ms_dom / n_dom, "traffic": None}
+    else:
+        by_launch = (stf["bytes_by_kind"][dom] + stb["bytes_by_kind"][dom]) / max(1, kernels[dom]["launches_per_step"])
+        achieved = by_launch / (ms_dom / n_dom / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_source": f"{pk['source']} hbm_gbs",
+                "bytes_per_launch": by_launch, "ms_per_launch": ms_dom / n_dom, "traffic": None}
+    launches = (stf["launches"] + stb["launches"]) * args.steps
+
+    # ---------------- end to end through the public API, host buffers ----------------
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: v.pin_memory() for k, v in host.items()}
+        outs = {"Y": torch.empty_like(Y, device="cpu").pin_memory(), "dX": torch.empty_like(dX, device="cpu").pin_memory(),
+                "dW_qkv": torch.empty_like(dWqkv, device="cpu").pin_memory(),
+                "dW_o": torch.empty_like(dWo, device="cpu").pin_memory()}
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = sum(v.numel() * v.element_size() for v in outs.values())
+
+        def e2e_step():
+            for k in pin:
+                d[k].copy_(pin[k], non_blocking=True)
+            step()
+            outs["Y"].copy_(Y, non_blocking=True)
+            outs["dX"].copy_(dX, non_blocking=True)
+            outs["dW_qkv"].copy_(dWqkv, non_blocking=True)
+            outs["dW_o"].copy_(dWo, non_blocking=True)
+        e2e_step()
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        barrier()
+        e_ms = f0.elapsed_time(f1)
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * sh.S * args.steps / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps}
+        upipe.sync_status()
+
+    mem_peak = torch.cuda.max_memory_allocated(dev) - mem_before
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        dt, v = oracle_sample(sh, args.cpu_sample_tokens)
+        cpu = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"fp64 numpy oracle fwd+bwd at the workload's widths with S={args.cpu_sample_tokens} "
+                         f"({dt:.1f} s), extrapolated to S={sh.S} by the model-FLOP ratio"}
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(args, sh),
+        "tflops": tflops, "frac_of_bf16_peak": tflops / peak_tf,
+        "peak_source": f"{pk['source']} bf16_tflops_sustained={peak_tf}",
+        "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clk,
+        "memory": {"stage_arena_bytes": stf["arena_peak_bytes"], "stage_arena_bwd_bytes": stb["arena_peak_bytes"],
+                   "closed_form_12SUd": stf["stage_closed_form_bytes"], "persistent_fwd_bytes": stf["persistent_bytes"],
+                   "persistent_bwd_bytes": stb["persistent_bytes"], "torch_peak_alloc_bytes": mem_peak,
+                   "permute_bytes_per_step": stf["permute_bytes"] + stb["permute_bytes"]},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

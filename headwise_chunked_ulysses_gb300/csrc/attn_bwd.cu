@@ -1,0 +1,466 @@
+// Causal GQA attention backward for the heads one stage holds.
+//
+// The pages describe only the forward stage; the backward pass here is the
+// analytic gradient of the same attention ("Untied Ulysses" summary, Method
+// steps (3)), recomputing P from the saved log-sum-exp:
+//   P  = exp(Q K^T / sqrt(d) - lse)          (causal)
+//   dV = sum over query heads sharing the KV head of P^T dO
+//   dS = P * (dO V^T - rowsum(dO * O))
+//   dQ = dS K / sqrt(d),  dK = sum over those query heads of dS^T Q / sqrt(d)
+//
+// One CTA per (KV slot, 128-row KV block).  It walks every query slot mapped
+// to its KV slot and every query block at or after its KV block, so the GQA
+// reduction of dK/dV happens in TMEM with no atomics.  Per step:
+//   S^T = K Q^T, dP^T = V dO^T  (tensor cores -> TMEM)
+//   warps 4..7 (one KV row each): P^T -> smem, then dS^T -> smem (same buffer)
+//   dV += P^T dO, dK += dS^T Q, dQ = dS K  (tensor cores; dQ reuses dP's TMEM)
+//   warps 8..11 (one query row each): dQ -> fp32 vector atomics into global.
+#include <cmath>
+
+#include "ptx.cuh"
+#include "upipe_internal.h"
+
+namespace upipe {
+namespace {
+
+constexpr int BQ = 128;
+constexpr int BKV = 128;
+constexpr int CH = 128 * 128;  // a 64-column chunk of a 128-row bf16 tile
+
+struct BwdArgs {
+  int S, n_qslots, n_kvslots, q_blocks;
+  float scale_log2, scale;
+  int accumulate_kv;
+  uint16_t kv_slot[kMaxSlots];
+  const float* lse2;
+  const float* Dsum;
+  float* dQacc;
+  float* dK;
+  float* dV;
+  int* status;
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int TILE = 128 * D * 2;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = TILE;
+  static constexpr int Q_OFF = 2 * TILE;    // 2 stages
+  static constexpr int DO_OFF = 4 * TILE;   // 2 stages
+  static constexpr int PDS_OFF = 6 * TILE;  // 128 x 128 bf16, P^T then dS^T
+  static constexpr int LSE_OFF = PDS_OFF + BKV * BQ * 2;  // 2 stages x 128 fp32
+  static constexpr int DS_OFF = LSE_OFF + 2 * BQ * 4;     // 2 stages x 128 fp32
+  static constexpr int BAR_OFF = DS_OFF + 2 * BQ * 4;
+  static constexpr int SMEM = BAR_OFF + 256;
+  // TMEM: S^T [0,128)  dP^T / dQ [128,256)  dV [256,256+D)  dK [256+D,256+2D)
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+};
+
+// The (query slot, query block) pairs a CTA visits, in order.
+struct ItemCursor {
+  int qs = -1, qb = 0, kvb = 0, q_blocks = 0;
+  __device__ bool next(const BwdArgs& a, int kvs) {
+    if (qs >= 0 && ++qb < q_blocks) return true;
+    for (++qs; qs < a.n_qslots; ++qs)
+      if (a.kv_slot[qs] == kvs) { qb = kvb; return true; }
+    return false;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                    const __grid_constant__ BwdArgs a) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* qdo_full = bars + 1;   // [2]
+  uint64_t* qdo_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;
+  uint64_t* dp_full = bars + 6;
+  uint64_t* p_ready = bars + 7;
+  uint64_t* p_consumed = bars + 8;
+  uint64_t* ds_ready = bars + 9;
+  uint64_t* ds_consumed = bars + 10;
+  uint64_t* dq_full = bars + 11;
+  uint64_t* dq_drained = bars + 12;
+  uint64_t* kv_done = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* s_lse = reinterpret_cast<float*>(smem + C::LSE_OFF);
+  float* s_D = reinterpret_cast<float*>(smem + C::DS_OFF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Watch w{abort_flag, a.status};
+  const bool aligned = (smem_u32(smem) & 1023u) == 0;
+
+  const int kvb = static_cast<int>(blockIdx.x) / a.n_kvslots;  // block 0 (most work) first
+  const int kvs = static_cast<int>(blockIdx.x) % a.n_kvslots;
+  int n_q = 0;
+  for (int i = 0; i < a.n_qslots; ++i) n_q += (a.kv_slot[i] == kvs);
+  const int n_items = n_q * (a.q_blocks - kvb);
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&qdo_full[s], 1);
+      mbar_init(&qdo_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(p_consumed, 1);
+    mbar_init(ds_ready, 128);
+    mbar_init(ds_consumed, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_drained, 128);
+    mbar_init(kv_done, 1);
+    *abort_flag = aligned ? 0 : 1;
+    if (!aligned && a.status) atomicCAS(a.status, 0, kDevBadSmem);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (aligned && n_items > 0) {
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer ----------------
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      tma_prefetch_map(&tmdO);
+      const int kv_row = kvs * a.S + kvb * BKV;
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_2d(smem + C::K_OFF + c * CH, &tmK, kv_full, c * 64, kv_row);
+        tma_load_2d(smem + C::V_OFF + c * CH, &tmV, kv_full, c * 64, kv_row);
+      }
+      ItemCursor cur;
+      cur.kvb = kvb;
+      cur.q_blocks = a.q_blocks;
+      for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
+        const int st = i & 1;
+        if (!mbar_wait(&qdo_empty[st], ((i >> 1) & 1) ^ 1, w, 40)) break;
+        const long long q_row = static_cast<long long>(cur.qs) * a.S + cur.qb * BQ;
+        mbar_arrive_expect_tx(&qdo_full[st], 2 * C::TILE + 2 * BQ * 4);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_2d(smem + C::Q_OFF + st * C::TILE + c * CH, &tmQ, &qdo_full[st], c * 64, (int)q_row);
+          tma_load_2d(smem + C::DO_OFF + st * C::TILE + c * CH, &tmdO, &qdo_full[st], c * 64, (int)q_row);
+        }
+        bulk_load(s_lse + st * BQ, a.lse2 + q_row, BQ * 4, &qdo_full[st]);
+        bulk_load(s_D + st * BQ, a.Dsum + q_row, BQ * 4, &qdo_full[st]);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t ID_S = idesc_bf16(BKV, BQ, false, false);  // S^T, dP^T
+      constexpr uint32_t ID_KV = idesc_bf16(BKV, D, false, true);   // dV, dK
+      constexpr uint32_t ID_Q = idesc_bf16(BQ, D, true, true);      // dQ
+      const uint32_t sK = smem_u32(smem + C::K_OFF);
+      const uint32_t sV = smem_u32(smem + C::V_OFF);
+      const uint32_t sPdS = smem_u32(smem + C::PDS_OFF);
+      auto sQ = [&](int st) { return smem_u32(smem + C::Q_OFF + st * C::TILE); };
+      auto sdO = [&](int st) { return smem_u32(smem + C::DO_OFF + st * C::TILE); };
+      auto qk_mma = [&](uint32_t d_tmem, uint32_t sA, uint32_t sB) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * CH + (k & 3) * 32;
+          mma_ss(d_tmem, sdesc_kmajor(sA + off), sdesc_kmajor(sB + off), ID_S, k > 0);
+        }
+      };
+      bool ok = mbar_wait(kv_full, 0, w, 41) && mbar_wait(&qdo_full[0], 0, w, 42);
+      if (ok) {
+        tc_fence_after();
+        qk_mma(tmem + C::T_S, sK, sQ(0));
+        mma_commit(s_full);
+        qk_mma(tmem + C::T_DP, sV, sdO(0));
+        mma_commit(dp_full);
+      }
+      for (int i = 0; ok && i < n_items; ++i) {
+        const int st = i & 1;
+        // dV += P^T dO
+        if (!mbar_wait(p_ready, i & 1, w, 43)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k) {
+          const uint32_t poff = (k >> 2) * CH + (k & 3) * 32;
+          mma_ss(tmem + C::T_DV, sdesc_kmajor(sPdS + poff), sdesc_mnmajor(sdO(st) + k * 2048, CH), ID_KV,
+                 (i | k) != 0);
+        }
+        mma_commit(p_consumed);
+        // next S^T (the softmax warps have read this one)
+        if (i + 1 < n_items) {
+          if (!mbar_wait(&qdo_full[st ^ 1], ((i + 1) >> 1) & 1, w, 44)) break;
+          tc_fence_after();
+          qk_mma(tmem + C::T_S, sK, sQ(st ^ 1));
+          mma_commit(s_full);
+        }
+        // dK += dS^T Q ; dQ = dS K (into dP's columns, read already)
+        if (!mbar_wait(ds_ready, i & 1, w, 45)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k) {
+          const uint32_t poff = (k >> 2) * CH + (k & 3) * 32;
+          mma_ss(tmem + C::T_DK, sdesc_kmajor(sPdS + poff), sdesc_mnmajor(sQ(st) + k * 2048, CH), ID_KV,
+                 (i | k) != 0);
+        }
+#pragma unroll
+        for (int k = 0; k < BKV / 16; ++k)
+          mma_ss(tmem + C::T_DP, sdesc_mnmajor(sPdS + k * 2048, CH), sdesc_mnmajor(sK + k * 2048, CH), ID_Q, k > 0);
+        mma_commit(ds_consumed);
+        mma_commit(dq_full);
+        mma_commit(&qdo_empty[st]);
+        // next dP^T once dQ has been drained out of its columns
+        if (i + 1 < n_items) {
+          if (!mbar_wait(dq_drained, i & 1, w, 46)) break;
+          tc_fence_after();
+          qk_mma(tmem + C::T_DP, sV, sdO(st ^ 1));
+          mma_commit(dp_full);
+        }
+      }
+      if (ok) mma_commit(kv_done);
+    } else if (warp >= 4 && warp < 8) {
+      // ---------------- P^T and dS^T: one KV row per thread ----------------
+      const int q4 = warp & 3;
+      const int row = q4 * 32 + lane;
+      const int kv_idx = kvb * BKV + row;
+      const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+      const uint32_t sPdS = smem_u32(smem + C::PDS_OFF);
+      const float sl2 = a.scale_log2;
+      ItemCursor cur;
+      cur.kvb = kvb;
+      cur.q_blocks = a.q_blocks;
+      bool ok = true;
+      for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
+        const int st = i & 1;
+        const bool diag = (cur.qb == kvb);
+        if (!mbar_wait_warp(s_full, i & 1, w, 47)) { ok = false; break; }
+        if (!mbar_wait_warp(&qdo_full[st], (i >> 1) & 1, w, 48)) { ok = false; break; }
+        tc_fence_after();
+        const float* lse = s_lse + st * BQ;
+        const float* Dv = s_D + st * BQ;
+        uint32_t pk[BQ / 2];
+#pragma unroll
+        for (int c = 0; c < BQ / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + C::T_S + c * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int q0 = c * 32 + e;
+            float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, -lse[q0]));
+            float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -lse[q0 + 1]));
+            if (diag) {
+              if (q0 < row) p0 = 0.f;
+              if (q0 + 1 < row) p1 = 0.f;
+            }
+            pk[(c * 32 + e) >> 1] = pack_bf16(p0, p1);
+          }
+        }
+        // the shared P/dS buffer is free once the previous step's dK and dQ MMAs are done
+        if (i > 0 && !mbar_wait_warp(ds_consumed, (i - 1) & 1, w, 49)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int piece = 0; piece < 8; ++piece) {
+            const int b = c * 32 + piece * 4;
+            st_shared_v4(sPdS + c * CH + row * 128 + ((piece ^ (row & 7)) << 4), pk[b], pk[b + 1], pk[b + 2],
+                         pk[b + 3]);
+          }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(p_ready);
+        // dS^T = P^T * (dP^T - D)
+        if (!mbar_wait_warp(dp_full, i & 1, w, 50)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < BQ / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + C::T_DP + c * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int q0 = c * 32 + e;
+            const uint32_t pp = pk[q0 >> 1];
+            const float d0 = bf16_lo(pp) * (__uint_as_float(v[e]) - Dv[q0]);
+            const float d1 = bf16_hi(pp) * (__uint_as_float(v[e + 1]) - Dv[q0 + 1]);
+            pk[q0 >> 1] = pack_bf16(d0, d1);
+          }
+        }
+        tc_fence_before();
+        if (!mbar_wait_warp(p_consumed, i & 1, w, 51)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int piece = 0; piece < 8; ++piece) {
+            const int b = c * 32 + piece * 4;
+            st_shared_v4(sPdS + c * CH + row * 128 + ((piece ^ (row & 7)) << 4), pk[b], pk[b + 1], pk[b + 2],
+                         pk[b + 3]);
+          }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_ready);
+      }
+      // dK, dV epilogue
+      if (ok && mbar_wait_warp(kv_done, 0, w, 52)) {
+        tc_fence_after();
+        const long long base = (static_cast<long long>(kvs) * a.S + kv_idx) * D;
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          float* dst = (which == 0 ? a.dV : a.dK) + base;
+          const float mul = which == 0 ? 1.f : a.scale;
+          const uint32_t col = which == 0 ? C::T_DV : C::T_DK;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + col + c * 32, v);
+            float4* o = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float4 x = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
+                                     __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
+              if (a.accumulate_kv) {
+                const float4 p = o[e];
+                x.x += p.x; x.y += p.y; x.z += p.z; x.w += p.w;
+              }
+              o[e] = x;
+            }
+          }
+        }
+      }
+    } else if (warp >= 8) {
+      // ---------------- dQ drain: one query row per thread ----------------
+      const int q4 = warp & 3;
+      const int row = q4 * 32 + lane;
+      const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+      ItemCursor cur;
+      cur.kvb = kvb;
+      cur.q_blocks = a.q_blocks;
+      for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
+        if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
+        tc_fence_after();
+        float* dst = a.dQacc + (static_cast<long long>(cur.qs) * a.S + cur.qb * BQ + row) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + C::T_DP + c * 32, v);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            red_add_v4(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]) * a.scale,
+                       __uint_as_float(v[4 * e + 1]) * a.scale, __uint_as_float(v[4 * e + 2]) * a.scale,
+                       __uint_as_float(v[4 * e + 3]) * a.scale);
+        }
+        tc_fence_before();
+        mbar_arrive(dq_drained);
+      }
+    }
+  } else if (aligned && n_items == 0 && !a.accumulate_kv && warp >= 4 && warp < 8) {
+    // a KV slot no query head uses in this launch: its gradient is zero
+    const int row = (warp & 3) * 32 + lane;
+    const long long base = (static_cast<long long>(kvs) * a.S + kvb * BKV + row) * D;
+    for (int c = 0; c < D; c += 4) {
+      *reinterpret_cast<float4*>(a.dK + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(a.dV + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// D = rowsum(dO * O) per (slot, token), lse in log2 units, dQ accumulator zeroed.
+__global__ void bwd_prep_kernel(const BwdPrepDesc p) {
+  const int lanes_per_row = p.D / 8;            // 16-byte vectors per row
+  const int rows_per_warp = 32 / lanes_per_row;
+  const int lane = threadIdx.x & 31;
+  const long long warp_g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long total = static_cast<long long>(p.n_slots) * p.S;
+  const long long r = warp_g * rows_per_warp + lane / lanes_per_row;
+  const int v = lane % lanes_per_row;
+  float acc = 0.f;
+  int slot = 0, t = 0;
+  if (r < total) {
+    slot = static_cast<int>(r / p.S);
+    t = static_cast<int>(r % p.S);
+    const uint4 x = *reinterpret_cast<const uint4*>(p.dO + t * p.ld_do +
+                                                    static_cast<long long>(p.do_unit[slot]) * p.D + v * 8);
+    const uint4 y = *reinterpret_cast<const uint4*>(p.O + t * p.ld_o +
+                                                    static_cast<long long>(p.o_unit[slot]) * p.D + v * 8);
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc += bf16_lo(xs[i]) * bf16_lo(ys[i]) + bf16_hi(xs[i]) * bf16_hi(ys[i]);
+    float4* z = reinterpret_cast<float4*>(p.dQacc + r * p.D + v * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int off = lanes_per_row / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (r < total && v == 0) {
+    p.Dsum[r] = acc;
+    p.lse2[r] = p.lse[static_cast<long long>(p.lse_row[slot]) * p.S + t] * 1.4426950408889634f;
+  }
+}
+
+template <int D>
+cudaError_t run_bwd(const CUtensorMap* tm, const BwdArgs& args, cudaStream_t st) {
+  auto kern = attn_bwd_kernel<D>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  kern<<<args.n_kvslots * args.q_blocks, 384, BwdCfg<D>::SMEM, st>>>(tm[0], tm[1], tm[2], tm[3], args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(const BwdPrepDesc& p, cudaStream_t st) {
+  if ((p.D != 64 && p.D != 128) || p.n_slots <= 0 || p.n_slots > kMaxSlots) return cudaErrorInvalidValue;
+  const long long rows = static_cast<long long>(p.n_slots) * p.S;
+  const int rows_per_warp = 32 / (p.D / 8);
+  const long long warps = (rows + rows_per_warp - 1) / rows_per_warp;
+  const long long blocks = (warps + 7) / 8;
+  bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) {
+  if ((d.D != 64 && d.D != 128) || d.S % 128 || d.n_qslots <= 0 || d.n_qslots > kMaxSlots ||
+      d.n_kvslots <= 0)
+    return cudaErrorInvalidValue;
+  CUtensorMap tm[4];
+  if (!make_tmap_bf16(&tm[0], d.Q, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tm[1], d.K, d.D, (uint64_t)d.n_kvslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tm[2], d.V, d.D, (uint64_t)d.n_kvslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tm[3], d.dO, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
+  BwdArgs a;
+  a.S = d.S;
+  a.n_qslots = d.n_qslots;
+  a.n_kvslots = d.n_kvslots;
+  a.q_blocks = d.S / BQ;
+  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.D)));
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.D)));
+  a.accumulate_kv = d.accumulate_kv;
+  for (int i = 0; i < d.n_qslots; ++i) a.kv_slot[i] = d.kv_slot[i];
+  a.lse2 = d.lse2;
+  a.Dsum = d.Dsum;
+  a.dQacc = d.dQacc;
+  a.dK = d.dK;
+  a.dV = d.dV;
+  a.status = status;
+  return d.D == 128 ? run_bwd<128>(tm, a, st) : run_bwd<64>(tm, a, st);
+}
+
+}  // namespace upipe

@@ -1,0 +1,276 @@
+// Dense bf16 contraction on the 5th-generation tensor cores.
+//
+// Serves the layer's projections: the per-stage QKV projection X * W_qkv[:,
+// stage heads] ("Untied Ulysses" summary, Method steps (1)), the per-stage
+// output-projection share O_s * W_o[stage rows] that each stage adds into Y,
+// and the matching backward contractions (dO, dX, dW_qkv, dW_o).
+//
+// Design: persistent CTAs (one per SM), 128 x BN output tiles, K in blocks of
+// 64.  Warp 0 issues TMA loads of 64x64 bf16 boxes (128-byte swizzle) into a
+// STAGES-deep shared-memory ring; warp 1 issues tcgen05.mma (M=128, N=BN,
+// K=16) into one of two TMEM accumulators; warps 4..7 drain the other
+// accumulator (tcgen05.ld) and write the epilogue, so the epilogue of tile t
+// overlaps the main loop of tile t+1.  Every box coordinate passes through an
+// optional 64-block gather map, which is how the non-contiguous head sets of
+// the out-of-order schedule are read without copies.
+#include <algorithm>
+
+#include "ptx.cuh"
+#include "upipe_internal.h"
+
+namespace upipe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int BOX_BYTES = 64 * 64 * 2;  // one 64x64 bf16 box: 64 rows of 128 B
+
+struct GemmArgs {
+  int M, N, K;
+  int m_tiles, n_tiles;
+  int use_amap_k, use_bmap_k, use_bmap_n, use_omap_n;
+  uint16_t amap_k[kMaxMap];
+  uint16_t bmap_k[kMaxMap];
+  uint16_t bmap_n[kMaxMap];
+  uint16_t omap_n[kMaxMap];
+  void* out;
+  long long ldo;
+  int out_mode;
+  const float* aux;
+  long long ld_aux;
+  int* status;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int SMEM = BAR_OFF + 256;
+};
+
+__device__ __forceinline__ void store_tile_chunk(const GemmArgs& g, int m, int oc, const uint32_t (&v)[32]) {
+  if (g.out_mode == kOutF32 || g.out_mode == kOutF32Acc) {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(g.out) + (long long)m * g.ldo + oc);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float4 x = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                             __uint_as_float(v[4 * i + 3]));
+      if (g.out_mode == kOutF32Acc) {
+        const float4 p = o[i];
+        x.x += p.x; x.y += p.y; x.z += p.z; x.w += p.w;
+      }
+      o[i] = x;
+    }
+  } else {
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+    if (g.out_mode == kOutBf16PlusF32) {
+      const float4* a = reinterpret_cast<const float4*>(g.aux + (long long)m * g.ld_aux + oc);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 p = a[i];
+        f[4 * i] += p.x; f[4 * i + 1] += p.y; f[4 * i + 2] += p.z; f[4 * i + 3] += p.w;
+      }
+    }
+    uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(g.out) + (long long)m * g.ldo + oc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[i] = make_uint4(pack_bf16(f[8 * i], f[8 * i + 1]), pack_bf16(f[8 * i + 2], f[8 * i + 3]),
+                        pack_bf16(f[8 * i + 4], f[8 * i + 5]), pack_bf16(f[8 * i + 6], f[8 * i + 7]));
+    }
+  }
+}
+
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(256, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ GemmArgs g) {
+  using C = Cfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Watch w{abort_flag, g.status};
+  const bool aligned = (smem_u32(smem) & 1023u) == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    *abort_flag = aligned ? 0 : 1;
+    if (!aligned && g.status) atomicCAS(g.status, 0, kDevBadSmem);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_tiles = g.m_tiles * g.n_tiles;
+  const int kblocks = g.K / BK;
+
+  if (aligned) {
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer ----------------
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        const int m0 = (t / g.n_tiles) * BM, n0 = (t % g.n_tiles) * BN;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, w, 1)) { ok = false; break; }
+          uint8_t* sa = smem + s * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::A_BYTES;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          const int ka = (g.use_amap_k ? g.amap_k[kb] : kb) * BK;
+          const int kbb = (g.use_bmap_k ? g.bmap_k[kb] : kb) * BK;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if (A_MN) tma_load_2d(sa + i * BOX_BYTES, &tmA, &full[s], m0 + 64 * i, ka);
+            else      tma_load_2d(sa + i * BOX_BYTES, &tmA, &full[s], ka, m0 + 64 * i);
+          }
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i) {
+            const int nb = n0 / 64 + i;
+            const int nc = (g.use_bmap_n ? g.bmap_n[nb] : nb) * 64;
+            if (B_MN) tma_load_2d(sb + i * BOX_BYTES, &tmB, &full[s], nc, kbb);
+            else      tma_load_2d(sb + i * BOX_BYTES, &tmB, &full[s], kbb, nc);
+          }
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+      int it = 0, tl = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++tl) {
+        const int acc = tl & 1;
+        if (!mbar_wait(&tempty[acc], ((tl >> 1) & 1) ^ 1, w, 2)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * BN;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&full[s], (it / STAGES) & 1, w, 3)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = A_MN ? sdesc_mnmajor(sa + k * 2048, BOX_BYTES) : sdesc_kmajor(sa + k * 32);
+            const uint64_t bd = B_MN ? sdesc_mnmajor(sb + k * 2048, BOX_BYTES) : sdesc_kmajor(sb + k * 32);
+            mma_ss(d_tmem, ad, bd, IDESC, (kb | k) != 0);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (ok) mma_commit(&tfull[acc]);
+      }
+    } else if (warp >= 4) {
+      // ---------------- epilogue (4 warps, one TMEM lane quarter each) ----------------
+      const int q = warp & 3;
+      const int row = q * 32 + lane;
+      int tl = 0;
+      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tl) {
+        const int acc = tl & 1;
+        if (!mbar_wait_warp(&tfull[acc], (tl >> 1) & 1, w, 4)) break;
+        tc_fence_after();
+        const int m = (t / g.n_tiles) * BM + row;
+        const int n0 = (t % g.n_tiles) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 32, v);
+          const int n = n0 + c * 32;
+          const int oc = g.use_omap_n ? g.omap_n[n >> 6] * 64 + (n & 63) : n;
+          store_tile_chunk(g, m, oc, v);
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int BN, bool A_MN, bool B_MN>
+cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, cudaStream_t st) {
+  auto kern = gemm_kernel<BN, A_MN, B_MN>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int tiles = args.m_tiles * args.n_tiles;
+  const int grid = std::min(tiles, num_sms());
+  kern<<<grid, 256, Cfg<BN>::SMEM, st>>>(ta, tb, args);
+  return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t dispatch_major(const GemmDesc& d, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                           cudaStream_t st) {
+  if (d.a_mn && d.b_mn) return run<BN, true, true>(ta, tb, a, st);
+  if (d.a_mn) return run<BN, true, false>(ta, tb, a, st);
+  if (d.b_mn) return run<BN, false, true>(ta, tb, a, st);
+  return run<BN, false, false>(ta, tb, a, st);
+}
+
+void copy_map(const BlockMap& m, int& use, uint16_t* dst) {
+  use = m.n > 0;
+  for (int i = 0; i < m.n && i < kMaxMap; ++i) dst[i] = m.idx[i];
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmDesc& d, int* status, cudaStream_t st) {
+  if (d.M % BM || d.K % BK || d.N % 64 || d.M <= 0 || d.N <= 0 || d.K <= 0) return cudaErrorInvalidValue;
+  const int BN = (d.N % 256 == 0) ? 256 : (d.N % 128 == 0 ? 128 : 64);
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16(&ta, d.A, d.a_cols, d.a_rows, d.lda, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, d.B, d.b_cols, d.b_rows, d.ldb, 64, 64)) return cudaErrorInvalidValue;
+  GemmArgs a;
+  a.M = d.M; a.N = d.N; a.K = d.K;
+  a.m_tiles = d.M / BM;
+  a.n_tiles = d.N / BN;
+  copy_map(d.amap_k, a.use_amap_k, a.amap_k);
+  copy_map(d.bmap_k, a.use_bmap_k, a.bmap_k);
+  copy_map(d.bmap_n, a.use_bmap_n, a.bmap_n);
+  copy_map(d.omap_n, a.use_omap_n, a.omap_n);
+  a.out = d.out; a.ldo = d.ldo; a.out_mode = d.out_mode;
+  a.aux = d.aux; a.ld_aux = d.ld_aux;
+  a.status = status;
+  if (BN == 256) return dispatch_major<256>(d, ta, tb, a, st);
+  if (BN == 128) return dispatch_major<128>(d, ta, tb, a, st);
+  return dispatch_major<64>(d, ta, tb, a, st);
+}
+
+}  // namespace upipe

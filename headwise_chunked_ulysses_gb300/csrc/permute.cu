@@ -1,0 +1,96 @@
+// The Ulysses all-to-all of C virtual ranks on one GPU, as an HBM permute.
+//
+// "Untied Ulysses" summary, Background (DeepSpeed Ulysses) and Method steps
+// (2) and (4): before attention each rank holds S/C tokens of every head of
+// the stage and needs all S tokens of U/C heads; afterwards the outputs go
+// back.  With the C ranks' buffers side by side in one GPU's memory, the
+// exchange is the index map
+//     seq layout  [S tokens][heads][d]    (rank c owns tokens cS/C..(c+1)S/C-1)
+//     head layout [slot][S tokens][d]     (rank c owns a run of slots)
+// and every byte moves once.  Each thread copies one 16-byte vector (8 bf16),
+// consecutive threads walk along d then along tokens, so both the reads and
+// the writes are full, coalesced 128-byte lines.
+//
+// head2seq can sum several source slots into one output head (the copies of
+// a KV head's gradient held by different ranks), in fp32, in the listed
+// order, then rounds once to bf16 (round to nearest even).
+#include <algorithm>
+
+#include "ptx.cuh"
+#include "upipe_internal.h"
+
+namespace upipe {
+namespace {
+
+__global__ void seq2head_kernel(const Seq2HeadDesc p) {
+  const int vpr = p.D / 8;  // 16-byte vectors per head row
+  const long long total = static_cast<long long>(p.n_slots) * p.S * vpr;
+  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int v = static_cast<int>(g % vpr);
+    const long long rest = g / vpr;
+    const int t = static_cast<int>(rest % p.S);
+    const int k = static_cast<int>(rest / p.S);
+    const uint4 x =
+        *reinterpret_cast<const uint4*>(p.src + t * p.ld_src + static_cast<long long>(p.src_head[k]) * p.D + v * 8);
+    *reinterpret_cast<uint4*>(p.dst + g * 8) = x;
+  }
+}
+
+template <bool F32>
+__global__ void head2seq_kernel(const Head2SeqDesc p) {
+  const int vpr = p.D / 8;
+  const long long total = static_cast<long long>(p.n_heads) * p.S * vpr;
+  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int v = static_cast<int>(g % vpr);
+    const long long rest = g / vpr;
+    const int t = static_cast<int>(rest % p.S);
+    const int k = static_cast<int>(rest / p.S);
+    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int r = p.first[k]; r < p.first[k + 1]; ++r) {
+      const long long off = (static_cast<long long>(p.src_slot[r]) * p.S + t) * p.D + v * 8;
+      if (F32) {
+        const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(p.src) + off);
+        const float4 a = s[0], b = s[1];
+        f[0] += a.x; f[1] += a.y; f[2] += a.z; f[3] += a.w;
+        f[4] += b.x; f[5] += b.y; f[6] += b.z; f[7] += b.w;
+      } else {
+        const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.src) + off);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          f[2 * i] += bf16_lo(w[i]);
+          f[2 * i + 1] += bf16_hi(w[i]);
+        }
+      }
+    }
+    *reinterpret_cast<uint4*>(p.dst + t * p.ld_dst + static_cast<long long>(p.dst_head[k]) * p.D + v * 8) =
+        make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+  }
+}
+
+unsigned grid_for(long long work, int threads) {
+  const long long want = (work + threads - 1) / threads;
+  const long long cap = static_cast<long long>(num_sms()) * 16;
+  return static_cast<unsigned>(std::max(1LL, std::min(want, cap)));
+}
+
+}  // namespace
+
+cudaError_t launch_seq2head(const Seq2HeadDesc& p, cudaStream_t st) {
+  if (p.D % 8 || p.n_slots <= 0 || p.n_slots > kMaxSlots || p.S <= 0) return cudaErrorInvalidValue;
+  const long long work = static_cast<long long>(p.n_slots) * p.S * (p.D / 8);
+  seq2head_kernel<<<grid_for(work, 256), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_head2seq(const Head2SeqDesc& p, cudaStream_t st) {
+  if (p.D % 8 || p.n_heads <= 0 || p.n_heads > kMaxSlots || p.S <= 0) return cudaErrorInvalidValue;
+  const long long work = static_cast<long long>(p.n_heads) * p.S * (p.D / 8);
+  if (p.src_f32) head2seq_kernel<true><<<grid_for(work, 256), 256, 0, st>>>(p);
+  else head2seq_kernel<false><<<grid_for(work, 256), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace upipe

@@ -1,0 +1,112 @@
+// Internal interfaces between the host orchestration and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace upipe {
+
+constexpr int kMaxMap = 256;   // 64-wide blocks a gather map can name
+constexpr int kMaxSlots = 256; // head slots one attention launch can hold
+
+// A gather over 64-element blocks: block b of the logical operand comes from
+// block idx[b] of the stored tensor.  n == 0 means identity.
+struct BlockMap {
+  int n = 0;
+  uint16_t idx[kMaxMap];
+};
+
+enum GemmOut : int {
+  kOutBf16 = 0,        // out(bf16)  = acc
+  kOutF32 = 1,         // out(fp32)  = acc
+  kOutF32Acc = 2,      // out(fp32) += acc
+  kOutBf16PlusF32 = 3, // out(bf16)  = acc + aux(fp32)
+};
+
+// D[M,N] = A[M,K] * B[K,N], bf16 operands, fp32 accumulation.
+//   a_mn == false: A stored [M rows][K cols] (K contiguous), else [K rows][M cols].
+//   b_mn == false: B stored [N rows][K cols],                else [K rows][N cols].
+// lda/ldb are the stored row strides in elements.  amap_k / bmap_k gather
+// along K, bmap_n gathers along N, omap_n scatters output column blocks.
+struct GemmDesc {
+  const void* A = nullptr; long long lda = 0; long long a_rows = 0; long long a_cols = 0; bool a_mn = false;
+  const void* B = nullptr; long long ldb = 0; long long b_rows = 0; long long b_cols = 0; bool b_mn = false;
+  int M = 0, N = 0, K = 0;
+  BlockMap amap_k, bmap_k, bmap_n, omap_n;
+  void* out = nullptr; long long ldo = 0; int out_mode = kOutF32;
+  const float* aux = nullptr; long long ld_aux = 0;
+};
+
+struct AttnFwdDesc {
+  const void* Q = nullptr;  // [n_qslots][S][D] bf16
+  const void* K = nullptr;  // [n_kvslots][S][D] bf16
+  const void* V = nullptr;  // [n_kvslots][S][D] bf16
+  void* O = nullptr;        // [n_qslots][S][D] bf16
+  float* lse = nullptr;     // rows lse_row[slot], each S long
+  int S = 0, D = 0, n_qslots = 0, n_kvslots = 0;
+  uint16_t kv_slot[kMaxSlots];
+  uint16_t lse_row[kMaxSlots];
+};
+
+struct AttnBwdDesc {
+  const void* Q = nullptr;   // [n_qslots][S][D] bf16
+  const void* K = nullptr;   // [n_kvslots][S][D] bf16
+  const void* V = nullptr;   // [n_kvslots][S][D] bf16
+  const void* dO = nullptr;  // [n_qslots][S][D] bf16
+  const float* lse2 = nullptr;  // [n_qslots][S]  log2-domain log-sum-exp
+  const float* Dsum = nullptr;  // [n_qslots][S]  rowsum(dO * O)
+  float* dQacc = nullptr;    // [n_qslots][S][D] fp32, pre-zeroed, atomically accumulated (unscaled)
+  float* dK = nullptr;       // [n_kvslots][S][D] fp32
+  float* dV = nullptr;       // [n_kvslots][S][D] fp32
+  int accumulate_kv = 0;     // add into dK/dV instead of overwriting
+  int S = 0, D = 0, n_qslots = 0, n_kvslots = 0;
+  uint16_t kv_slot[kMaxSlots];  // q slot -> kv slot
+};
+
+// Copy of head blocks between sequence layout [S][row of heads] and head
+// layout [slot][S][D].
+struct Seq2HeadDesc {
+  const uint16_t* src = nullptr; long long ld_src = 0;  // elements per token row
+  uint16_t* dst = nullptr;                              // [n_slots][S][D]
+  int S = 0, D = 0, n_slots = 0;
+  uint16_t src_head[kMaxSlots];  // slot -> head block in a source row
+};
+struct Head2SeqDesc {
+  const void* src = nullptr; bool src_f32 = false;       // [*][S][D]
+  uint16_t* dst = nullptr; long long ld_dst = 0;         // bf16 [S][row]
+  int S = 0, D = 0, n_heads = 0;
+  uint16_t dst_head[kMaxSlots];     // output head -> head block in a dest row
+  uint16_t first[kMaxSlots + 1];    // CSR over source slots per output head
+  uint16_t src_slot[kMaxSlots];     // summed in this order (fp32)
+};
+struct BwdPrepDesc {
+  const uint16_t* dO = nullptr; long long ld_do = 0;  // seq layout
+  const uint16_t* O = nullptr; long long ld_o = 0;    // seq layout (saved forward output)
+  const float* lse = nullptr;                         // [*][S] natural log
+  float* Dsum = nullptr;   // [n_slots][S]
+  float* lse2 = nullptr;   // [n_slots][S]
+  float* dQacc = nullptr;  // [n_slots][S][D], zeroed here
+  int S = 0, D = 0, n_slots = 0;
+  // slot -> start of its d-wide block, in units of D elements: a head index
+  // for sequence layout, slot*S for head layout (with ld == D)
+  int32_t do_unit[kMaxSlots];
+  int32_t o_unit[kMaxSlots];
+  uint16_t lse_row[kMaxSlots];  // slot -> lse row
+};
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_gemm(const GemmDesc& g, int* status, cudaStream_t st);
+cudaError_t launch_attn_fwd(const AttnFwdDesc& a, int* status, cudaStream_t st);
+cudaError_t launch_attn_bwd(const AttnBwdDesc& a, int* status, cudaStream_t st);
+cudaError_t launch_seq2head(const Seq2HeadDesc& p, cudaStream_t st);
+cudaError_t launch_head2seq(const Head2SeqDesc& p, cudaStream_t st);
+cudaError_t launch_bwd_prep(const BwdPrepDesc& p, cudaStream_t st);
+
+// Tensor maps (driver entry point resolved through the runtime).
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
+                    uint32_t box_inner, uint32_t box_outer);
+int num_sms();
+
+}  // namespace upipe

@@ -1,0 +1,212 @@
+/*
+ * upipe.h -- C ABI of the headwise-chunked (UPipe) causal GQA attention layer
+ * on one GB300 (sm_103a).
+ *
+ * The operation is the attention layer of "Untied Ulysses: Memory-Efficient
+ * Context Parallelism via Headwise Chunking" (summary page, paper.rainbus.top):
+ *   - Core method: attention runs in H/U stages of U heads; the stage buffers
+ *     are reused, so intermediate memory grows with U, not H.
+ *   - Method steps (1)-(4): per stage, project X onto the Q, K, V of heads
+ *     iU..(i+1)U-1; all-to-all from sequence shards (S/C tokens per rank) to
+ *     head shards (U/C heads of all S tokens per rank); causal attention;
+ *     all-to-all back.  Each stage then adds its heads' share of the output
+ *     projection, O_s W_o[rows of s], into Y.
+ *   - Novelty: the GQA schedule takes heads out of order so every KV head is
+ *     exchanged once, in the first stage, and later stages move query heads only.
+ *   - Background: DeepSpeed Ulysses (the all-to-all) and GQA (H query heads
+ *     share G KV heads, H/G consecutive query heads per KV head).
+ * The C ranks are virtual: their buffers sit side by side in one GPU's memory
+ * and the all-to-all is a device permute with the same index map.
+ *
+ * Conventions for every call:
+ *   - All tensors are row-major.  bf16 values are passed as upipe_bf16 bit
+ *     patterns; fp32 as float.
+ *   - X, Y, dY, dX: [S, d_model].  W_qkv: [d_model, (H + 2G) d_head], columns
+ *     [Q head 0..H-1 | K head 0..G-1 | V head 0..G-1], d_head columns each.
+ *     W_o: [H d_head, d_model].  O_saved: [S, H d_head].  lse: [H, S], natural
+ *     log of each causal softmax row's normaliser (scores scaled 1/sqrt(d_head)).
+ *   - Pointers named as device pointers must be device memory the caller owns
+ *     and 16-byte aligned.  The library never allocates device memory and keeps
+ *     no pointer after a call returns.  Work is ordered on `stream` (a
+ *     cudaStream_t; NULL is the legacy default stream); calls return once the
+ *     work is enqueued.  Two calls may run concurrently only with distinct
+ *     workspaces and outputs.
+ *   - Return value: UPIPE_OK or an error code.  Argument checks happen before
+ *     any launch: on an error nothing has been enqueued, except for
+ *     UPIPE_ECUDA (a launch failed) and UPIPE_ETIMEOUT.
+ *   - Shape rules (method constraints and kernel tiling): U | H (stages of U
+ *     heads), C | U (U/C heads per rank; the pages' Limitations section),
+ *     G | H, C | S, S % 128 == 0, d_model % 128 == 0, d_head in {64, 128},
+ *     H + 2G <= 256 heads in one stage; the out-of-order schedule also needs
+ *     C | G or G | C.
+ */
+#ifndef UPIPE_H
+#define UPIPE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t upipe_bf16; /* bfloat16 storage */
+
+enum upipe_status {
+  UPIPE_OK = 0,
+  UPIPE_EINVAL = 1,      /* bad shape, null or misaligned pointer */
+  UPIPE_ENOSPC = 2,      /* workspace smaller than *_workspace_bytes() */
+  UPIPE_EUNSUPPORTED = 3,/* d_head not 64/128, or the GPU is not sm_103 */
+  UPIPE_ECUDA = 4,       /* a CUDA launch or runtime call failed */
+  UPIPE_ETIMEOUT = 5     /* a kernel's bounded wait gave up (device status word) */
+};
+
+enum upipe_schedule {
+  UPIPE_SCHED_INORDER = 0, /* stage i holds heads iU..(i+1)U-1; each query slot gets its KV head */
+  UPIPE_SCHED_GQA_OOO = 1  /* rank r keeps heads r*H/C..(r+1)*H/C-1; KV heads move once, stage 0 */
+};
+
+/* Kernel kinds, for the statistics and the optional timing below. */
+enum upipe_kernel_kind {
+  UPIPE_KERNEL_GEMM = 0,
+  UPIPE_KERNEL_ATTN_FWD = 1,
+  UPIPE_KERNEL_ATTN_BWD = 2,
+  UPIPE_KERNEL_SEQ2HEAD = 3,
+  UPIPE_KERNEL_HEAD2SEQ = 4,
+  UPIPE_KERNEL_BWD_PREP = 5,
+  UPIPE_KERNEL_KINDS = 6
+};
+
+/* Filled by the layer calls when `stats` is non-NULL. */
+typedef struct {
+  size_t arena_peak_bytes;        /* stage arena high-water mark of the call's slot plan */
+  size_t stage_closed_form_bytes; /* 12*S*U*d_head: the pages' QKV + exchange form, summed over C ranks */
+  size_t persistent_bytes;        /* workspace outside the stage arena (fp32 accumulators, resident KV) */
+  size_t permute_bytes;           /* bytes read + written by the emulated all-to-alls */
+  int launches;                   /* kernel launches enqueued */
+  int stages;                     /* H / U */
+  /* per kernel kind: launches, algorithmic FLOPs (GEMM 2MNK; attention 2*d per
+   * causal (query, key) pair and matmul: 2 matmuls forward, 5 backward) and
+   * algorithmic HBM bytes (operands read once, results written once) */
+  int launches_by_kind[UPIPE_KERNEL_KINDS];
+  double flops_by_kind[UPIPE_KERNEL_KINDS];
+  double bytes_by_kind[UPIPE_KERNEL_KINDS];
+} upipe_stats;
+
+/* Workspace sizes in bytes for the layer calls (0 if the shape is invalid). */
+size_t upipe_fwd_workspace_bytes(int S, int d_model, int H, int G, int d_head, int U, int C, int sched);
+size_t upipe_bwd_workspace_bytes(int S, int d_model, int H, int G, int d_head, int U, int C, int sched);
+
+/*
+ * Forward pass of the layer (Method steps (1)-(4) per stage, plus the
+ * stage's share of Y = O W_o).
+ *   X, W_qkv, W_o : device, bf16, inputs.
+ *   Y             : device, bf16 [S, d_model], output.
+ *   O_saved       : device, bf16 [S, H*d_head], output (attention output of every
+ *                   head, kept for the backward pass).
+ *   lse           : device, fp32 [H, S], output.
+ *   ws            : device workspace of at least upipe_fwd_workspace_bytes() bytes,
+ *                   256-byte aligned; contents on entry are ignored.
+ */
+int upipe_attn_fwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model,
+                   int H, int G, int d_head, int U, int C, int sched, upipe_bf16* Y, upipe_bf16* O_saved,
+                   float* lse, void* ws, size_t ws_bytes, void* stream, upipe_stats* stats);
+
+/*
+ * Backward pass: gradients of L = <Y, dY>.  The pages do not describe it; it
+ * runs the same stages, recomputing each stage's projection and exchange (Q,
+ * K, V are never kept), and uses O_saved and lse from the forward call.
+ *   dY      : device, bf16 [S, d_model], input.
+ *   dX      : device, bf16 [S, d_model], output.
+ *   dW_qkv  : device, fp32 [d_model, (H+2G) d_head], output.
+ *   dW_o    : device, fp32 [H d_head, d_model], output.
+ *   ws      : at least upipe_bwd_workspace_bytes() bytes.
+ */
+int upipe_attn_bwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model,
+                   int H, int G, int d_head, int U, int C, int sched, const upipe_bf16* O_saved,
+                   const float* lse, const upipe_bf16* dY, upipe_bf16* dX, float* dW_qkv, float* dW_o, void* ws,
+                   size_t ws_bytes, void* stream, upipe_stats* stats);
+
+/*
+ * The Ulysses input all-to-all over C virtual ranks (Background, DeepSpeed
+ * Ulysses; Method steps (2)).  src is sequence-sharded: device bf16 rows of
+ * src_row_stride elements, token t at row t, head h at columns h*d_head..;
+ * rank c owns tokens [c S/C, (c+1) S/C).  dst is head-sharded: device bf16
+ * [C][n_heads/C][S][d_head], rank c receiving heads c*n_heads/C .. +n_heads/C-1.
+ * Needs C | n_heads, C | S, d_head % 8 == 0, src_row_stride % 8 == 0.
+ */
+int upipe_layout_seq2head(const upipe_bf16* src, upipe_bf16* dst, int S, int n_heads, int d_head, int C,
+                          int src_row_stride, void* stream);
+
+/* The reverse exchange (Method steps (4)): head-sharded src
+ * [C][n_heads/C][S][d_head] back to sequence-sharded dst rows of
+ * dst_row_stride elements.  Same requirements. */
+int upipe_layout_head2seq(const upipe_bf16* src, upipe_bf16* dst, int S, int n_heads, int d_head, int C,
+                          int dst_row_stride, void* stream);
+
+/*
+ * Head schedule (Method steps (1)-(2), Novelty): host_out[(i*C + r)*(U/C) + j]
+ * receives the query head that stage i places in slot j of rank r.
+ * host_out is HOST memory of H int32 entries.
+ */
+int upipe_schedule_table(int H, int G, int U, int C, int sched, int32_t* host_out);
+
+/*
+ * Causal GQA attention of one stage's heads in head layout (Method steps (3)).
+ *   Q   : device bf16 [n_q][S][d_head];  K, V: device bf16 [n_kv][S][d_head].
+ *   kv_of_q : HOST int32 [n_q], the KV slot each query slot reads.
+ *   O   : device bf16 [n_q][S][d_head];  lse: device fp32 [n_q][S] (natural log).
+ * n_q <= 256, S % 128 == 0.
+ */
+int upipe_attention_fwd(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf16* V, int n_q, int n_kv, int S,
+                        int d_head, const int32_t* kv_of_q, upipe_bf16* O, float* lse, void* stream);
+
+/*
+ * Its backward pass.  dO: device bf16 [n_q][S][d_head]; O, lse from the forward.
+ *   dQ  : device fp32 [n_q][S][d_head], output.
+ *   dK, dV : device fp32 [n_kv][S][d_head], output (summed over the query
+ *            slots that share each KV slot).
+ *   ws  : device workspace of 8*n_q*S bytes.
+ */
+int upipe_attention_bwd(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf16* V, const upipe_bf16* O,
+                        const upipe_bf16* dO, const float* lse, int n_q, int n_kv, int S, int d_head,
+                        const int32_t* kv_of_q, float* dQ, float* dK, float* dV, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/*
+ * The dense contraction behind the projections (Method steps (1) and the
+ * output projection): D[M,N] = A[M,K] B[K,N], bf16 in, fp32 accumulate.
+ *   A : device bf16, stored [M][K] (a_trans == 0) or [K][M] (a_trans == 1), row stride lda.
+ *   B : device bf16, stored [K][N] (b_trans == 0) or [N][K] (b_trans == 1), row stride ldb.
+ *   out_mode 0: D bf16;  1: D fp32;  2: D fp32 += A B.  ldd: row stride of D.
+ * M % 128 == 0, N % 64 == 0, K % 64 == 0.
+ */
+int upipe_gemm_bf16(const upipe_bf16* A, const upipe_bf16* B, void* D, int M, int N, int K, int a_trans, int b_trans,
+                    long long lda, long long ldb, long long ldd, int out_mode, void* stream);
+
+/* Reads (and clears) the device status word that bounded waits write; the
+ * call synchronises `stream`.  UPIPE_OK or UPIPE_ETIMEOUT. */
+int upipe_sync_status(void* stream);
+
+/* Static description of a status code. */
+const char* upipe_status_str(int status);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int upipe_version(void);
+
+/*
+ * Optional kernel timing, off by default.  When enabled, every kernel the
+ * library enqueues is bracketed by two CUDA events on the caller's stream;
+ * upipe_profile_read() waits for them and returns, per kernel kind, the summed
+ * milliseconds and the launch count since the last read (or enable), then
+ * clears.  Output arrays: HOST memory of UPIPE_KERNEL_KINDS entries.  The
+ * events add a few microseconds per launch; leave timing off in production.
+ */
+int upipe_profile_enable(int on);
+int upipe_profile_read(double* ms_by_kind, int* count_by_kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UPIPE_H */

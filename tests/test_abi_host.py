@@ -1,0 +1,134 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and
+exports every declared entry point, the schedule table matches the oracle's
+enumeration bit for bit, the workspace plan follows the closed forms, and
+bad arguments are rejected before anything is launched."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import upipe_oracle as orc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def upipe():
+    import headwise_chunked_ulysses_gb300 as u
+    if not os.path.exists(u.LIB_PATH):
+        from headwise_chunked_ulysses_gb300 import _build
+        _build.build()
+    u.lib()
+    return u
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "upipe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(upipe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(upipe):
+    names = declared_functions()
+    assert len(names) >= 13
+    lib = ctypes.CDLL(upipe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(upipe.EXPORTS)
+
+
+@pytest.mark.parametrize("H,G,U,C", [(8, 2, 2, 2), (8, 2, 8, 4), (32, 8, 8, 8), (32, 8, 16, 8), (32, 8, 32, 8),
+                                     (64, 8, 8, 8), (12, 3, 6, 3), (32, 2, 8, 8), (8, 2, 1, 1), (8, 8, 4, 2)])
+def test_schedule_table_is_the_oracle_enumeration(upipe, H, G, U, C):
+    for sched in (upipe.IN_ORDER, upipe.GQA_OUT_OF_ORDER):
+        if sched == upipe.GQA_OUT_OF_ORDER and not (G % C == 0 or C % G == 0):
+            with pytest.raises(upipe.UpipeError):
+                upipe.schedule_table(H, G, U, C, sched)
+            continue
+        got = upipe.schedule_table(H, G, U, C, sched)
+        want = orc.stage_heads(H, G, U, C, sched)
+        assert got.dtype == np.int32
+        assert np.array_equal(got, want)
+
+
+def _arena_fwd(upipe, sh):
+    total = upipe.fwd_workspace_bytes(sh)
+    stages = sh.H // sh.U
+    return total - (sh.S * sh.d_model * 4 if stages > 1 else 0)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b_32k", "qwen3_32b_128k", "llama3_8b_256k_usweep"])
+def test_forward_arena_follows_the_closed_form(upipe, name):
+    from synthetic import SHAPES
+    s = SHAPES[name]
+    sh = upipe.Shape(s.S, s.d_model, s.H, s.G, s.d_head, s.U, s.C, upipe.IN_ORDER)
+    arena = _arena_fwd(upipe, sh)
+    closed = 12 * s.S * s.U * s.d_head          # the pages' per-rank form summed over C ranks
+    assert closed == s.C * orc.upipe_stage_bytes_per_rank(s.S, s.C, s.U, s.d_head)
+    assert arena <= closed + 1024
+    # with G = H (no head sharing) the plan meets the form exactly
+    mha = upipe.Shape(s.S, s.d_model, s.H, s.H, s.d_head, s.U, s.C, upipe.IN_ORDER)
+    assert abs(_arena_fwd(upipe, mha) - 12 * s.S * s.U * s.d_head) <= 1024
+
+
+def test_arena_scales_with_u_not_h(upipe):
+    S, dm, H, G, d, C = 262144, 4096, 32, 8, 128, 8
+    a = {U: _arena_fwd(upipe, upipe.Shape(S, dm, H, G, d, U, C)) for U in (8, 16, 32)}
+    assert a[16] / a[8] == pytest.approx(2.0, rel=0.01)
+    assert a[32] / a[8] == pytest.approx(4.0, rel=0.01)
+    # Qwen3-32B shape: U = 8 against Ulysses (U = H = 64): 1/8 of the memory, the pages' 87.5 %
+    q8 = _arena_fwd(upipe, upipe.Shape(131072, 5120, 64, 8, 128, 8, 8))
+    q64 = _arena_fwd(upipe, upipe.Shape(131072, 5120, 64, 8, 128, 64, 8))
+    assert 1 - q8 / q64 == pytest.approx(0.875, abs=0.01)
+
+
+def test_backward_arena_has_no_h_term(upipe):
+    # same group size H/G, twice the heads: same workspace
+    S, dm, d, U, C = 4096, 1024, 128, 8, 8
+    for sched in (upipe.IN_ORDER, upipe.GQA_OUT_OF_ORDER):
+        b32 = upipe.bwd_workspace_bytes(upipe.Shape(S, dm, 32, 8, d, U, C, sched))
+        b64 = upipe.bwd_workspace_bytes(upipe.Shape(S, dm, 64, 16, d, U, C, sched))
+        if sched == upipe.IN_ORDER:
+            assert b32 == b64
+        else:  # resident KV heads are O(G): per extra KV head, K and V in sequence
+            # layout (2+2 bytes), head layout (2+2) and their fp32 gradients (4+4)
+            assert b64 - b32 <= 8 * S * d * 16 + 4096
+
+
+def test_invalid_shapes_are_rejected(upipe):
+    bad = [
+        upipe.Shape(1024, 512, 8, 2, 64, 3, 1),     # U does not divide H
+        upipe.Shape(1024, 512, 8, 2, 64, 4, 3),     # C does not divide U
+        upipe.Shape(1000, 512, 8, 2, 64, 2, 2),     # S not a multiple of 128
+        upipe.Shape(1024, 500, 8, 2, 64, 2, 2),     # d_model not a multiple of 128
+        upipe.Shape(1024, 512, 8, 3, 64, 2, 2),     # G does not divide H
+        upipe.Shape(1024, 512, 8, 2, 96, 2, 2),     # unsupported head width
+        upipe.Shape(1536, 512, 12, 4, 64, 6, 3, 1),  # out of order needs C|G or G|C
+    ]
+    for sh in bad:
+        assert upipe.fwd_workspace_bytes(sh) == 0
+        assert upipe.bwd_workspace_bytes(sh) == 0
+
+
+def test_arguments_checked_before_any_launch(upipe):
+    lib = upipe.lib()
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # aligned, never dereferenced: every check below fails first
+    sh = upipe.Shape(1024, 512, 8, 2, 64, 2, 2)
+    need = upipe.fwd_workspace_bytes(sh)
+    st = upipe.Stats()
+    rc = lib.upipe_attn_fwd(fake, fake, fake, *sh.args(), fake, fake, fake, fake, need - 1, None, ctypes.byref(st))
+    assert rc == upipe.ENOSPC
+    rc = lib.upipe_attn_fwd(fake, fake, None, *sh.args(), fake, fake, fake, fake, need, None, ctypes.byref(st))
+    assert rc == upipe.EINVAL
+    rc = lib.upipe_attn_fwd(P((1 << 20) + 8), fake, fake, *sh.args(), fake, fake, fake, fake, need, None,
+                            ctypes.byref(st))
+    assert rc == upipe.EINVAL
+    rc = lib.upipe_attn_fwd(fake, fake, fake, 1024, 512, 8, 2, 64, 3, 1, 0, fake, fake, fake, fake, need, None,
+                            ctypes.byref(st))
+    assert rc == upipe.EINVAL
+    rc = lib.upipe_layout_seq2head(fake, fake, 1024, 6, 64, 4, 384, None)
+    assert rc == upipe.EINVAL
+    assert lib.upipe_status_str(upipe.ETIMEOUT) == b"a kernel wait timed out"

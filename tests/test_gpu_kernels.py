@@ -1,0 +1,139 @@
+"""Parity of the individual CUDA kernels, called through the C ABI.
+
+* the Ulysses exchange (seq->head, head->seq): bit-exact against the oracle's
+  all-to-all of C virtual ranks;
+* the tensor-core contraction in all four operand layouts and three output
+  modes: against an fp64 product of the same bf16 operands;
+* causal GQA attention forward and backward: against the oracle's attention
+  core (fp64), per head; dK, dV summed over the query heads of each group.
+"""
+import numpy as np
+import pytest
+
+from oracle import upipe_oracle as orc
+from synthetic import normal_bf16, bf16_bits_to_f64
+from tests.helpers import to_dev, bits_of, f64_of, rel
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def up():
+    import torch
+    import headwise_chunked_ulysses_gb300 as u
+    u.lib()
+    assert torch.cuda.is_available()
+    return u
+
+
+# ---------------------------------------------------------------------------
+# exchange
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("S,n_heads,d,C,pad", [(1024, 8, 64, 2, 0), (384, 6, 128, 3, 0), (256, 4, 64, 4, 64),
+                                               (512, 12, 128, 4, 128), (96, 3, 64, 3, 0)])
+def test_exchange_is_bit_exact(up, S, n_heads, d, C, pad):
+    import torch
+    rng = np.random.default_rng(S + n_heads + d + C)
+    ld = n_heads * d + pad
+    src_bits = rng.integers(0, 1 << 16, size=(S, ld), dtype=np.uint16)
+    src = to_dev(src_bits)
+    dst = torch.empty(n_heads, S, d, dtype=torch.bfloat16, device="cuda")
+    up.layout_seq2head(src, dst, S, n_heads, d, C, ld)
+    got = bits_of(dst)
+    Sc = S // C
+    shards = [{h: src_bits[c * Sc:(c + 1) * Sc, h * d:(h + 1) * d] for h in range(n_heads)} for c in range(C)]
+    per = n_heads // C
+    wanted = [list(range(r * per, (r + 1) * per)) for r in range(C)]
+    held = orc.seq_to_head(shards, wanted)
+    want = np.concatenate(held, axis=0)
+    assert np.array_equal(got, want)
+    # and back: every head lands in its columns, padding untouched
+    back_bits = rng.integers(0, 1 << 16, size=(S, ld), dtype=np.uint16)
+    back = to_dev(back_bits)
+    up.layout_head2seq(dst, back, S, n_heads, d, C, ld)
+    got_back = bits_of(back)
+    assert np.array_equal(got_back[:, :n_heads * d], src_bits[:, :n_heads * d])
+    assert np.array_equal(got_back[:, n_heads * d:], back_bits[:, n_heads * d:])
+
+
+# ---------------------------------------------------------------------------
+# contraction
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K", [(256, 384, 320), (128, 512, 128), (384, 64, 192), (256, 256, 1024)])
+@pytest.mark.parametrize("a_trans,b_trans", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_gemm_layouts_and_modes(up, M, N, K, a_trans, b_trans):
+    import torch
+    seed = M + N + K + 10 * a_trans + 20 * b_trans
+    A_bits = normal_bf16((K, M) if a_trans else (M, K), seed)
+    B_bits = normal_bf16((N, K) if b_trans else (K, N), seed + 1)
+    A64, B64 = bf16_bits_to_f64(A_bits), bf16_bits_to_f64(B_bits)
+    want = (A64.T if a_trans else A64) @ (B64.T if b_trans else B64)
+    A, B = to_dev(A_bits), to_dev(B_bits)
+    D32 = up.gemm(A, B, M, N, K, a_trans, b_trans, out_mode=1)
+    assert rel(f64_of(D32), want) < 1e-5
+    D16 = up.gemm(A, B, M, N, K, a_trans, b_trans, out_mode=0)
+    assert rel(f64_of(D16), want) < 1e-2
+    base = torch.randn(M, N, dtype=torch.float32, device="cuda")
+    base0 = f64_of(base)
+    up.gemm(A, B, M, N, K, a_trans, b_trans, out_mode=2, D=base)
+    assert rel(f64_of(base), base0 + want) < 1e-5
+    up.sync_status()
+
+
+# ---------------------------------------------------------------------------
+# attention core
+# ---------------------------------------------------------------------------
+
+def _attn_inputs(n_q, n_kv, S, d, seed):
+    Q = normal_bf16((n_q, S, d), seed)
+    K = normal_bf16((n_kv, S, d), seed + 1)
+    V = normal_bf16((n_kv, S, d), seed + 2)
+    dO = normal_bf16((n_q, S, d), seed + 3)
+    return Q, K, V, dO
+
+
+CASES = [(4, 2, 384, 64, [0, 0, 1, 1]), (4, 2, 256, 128, [0, 0, 1, 1]), (2, 2, 1024, 128, [0, 1]),
+         (3, 1, 128, 64, [0, 0, 0]), (2, 4, 512, 64, [3, 1])]
+
+
+@pytest.mark.parametrize("n_q,n_kv,S,d,kv", CASES)
+def test_attention_forward_and_backward(up, n_q, n_kv, S, d, kv):
+    Qb, Kb, Vb, dOb = _attn_inputs(n_q, n_kv, S, d, seed=S + d + n_q)
+    Q, K, V, dO = (to_dev(x) for x in (Qb, Kb, Vb, dOb))
+    O, lse = up.attention_fwd(Q, K, V, kv)
+    dQ, dK, dV = up.attention_bwd(Q, K, V, O, dO, lse, kv)
+    up.sync_status()
+    q64, k64, v64, do64 = (bf16_bits_to_f64(x) for x in (Qb, Kb, Vb, dOb))
+    Og, lseg, dQg, dKg, dVg = (f64_of(x) for x in (O, lse, dQ, dK, dV))
+    dK_ref = np.zeros_like(k64)
+    dV_ref = np.zeros_like(v64)
+    used = set(kv)
+    for h in range(n_q):
+        g = kv[h]
+        o, l, P = orc.attention_head_forward(q64[h], k64[g], v64[g])
+        assert rel(Og[h], o) < 1e-2, ("O", h)
+        assert np.abs(lseg[h] - l).max() < 2e-3, ("lse", h)
+        dq, dk, dv = orc.attention_head_backward(q64[h], k64[g], v64[g], P, o, do64[h])
+        assert rel(dQg[h], dq) < 1e-2, ("dQ", h)
+        dK_ref[g] += dk
+        dV_ref[g] += dv
+    for g in range(n_kv):
+        if g in used:
+            assert rel(dKg[g], dK_ref[g]) < 1e-2, ("dK", g)
+            assert rel(dVg[g], dV_ref[g]) < 1e-2, ("dV", g)
+        else:  # a KV slot no query reads has zero gradient
+            assert np.all(dKg[g] == 0) and np.all(dVg[g] == 0)
+
+
+def test_attention_first_row_copies_first_value(up):
+    # query 0 sees only key 0: O[0] = V[0] and lse[0] = q0.k0/sqrt(d), whatever the scores
+    import torch
+    S, d = 256, 128
+    Qb, Kb, Vb, _ = _attn_inputs(1, 1, S, d, seed=77)
+    O, lse = up.attention_fwd(to_dev(Qb), to_dev(Kb), to_dev(Vb), [0])
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_of(O)[0, 0], Vb[0, 0])
+    s00 = float(bf16_bits_to_f64(Qb)[0, 0] @ bf16_bits_to_f64(Kb)[0, 0]) / np.sqrt(d)
+    assert abs(f64_of(lse)[0, 0] - s00) < 1e-4

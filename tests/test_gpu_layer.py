@@ -1,0 +1,161 @@
+"""End-to-end parity of the layer (forward and backward) through the C ABI.
+
+The oracle is the plain fp64 layer: the method only regroups the work, so
+every U (including U = H, plain Ulysses), every C and both schedules must
+reproduce it.  Tolerance: relative Frobenius error <= 1e-2 on each of Y, dX,
+dW_qkv and dW_o (bf16 inputs, fp32 accumulation).  Also checked: the output
+guards and the workspace tail stay untouched, and the plan's statistics.
+"""
+import numpy as np
+import pytest
+
+from oracle import upipe_oracle as orc
+from synthetic import SHAPES, LayerShape, layer_inputs, bf16_bits_to_f64
+from tests.helpers import to_dev, f64_of, rel
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def up():
+    import headwise_chunked_ulysses_gb300 as u
+    u.lib()
+    return u
+
+
+class Ref:
+    def __init__(self, sh: LayerShape, seed=0, backward=True):
+        self.sh = sh
+        self.bits = layer_inputs(sh, seed)
+        f = {k: bf16_bits_to_f64(v) for k, v in self.bits.items()}
+        self.Y, self.O, self.lse = orc.layer_forward(f["X"], f["W_qkv"], f["W_o"], sh.H, sh.G, sh.d_head)
+        if backward:
+            self.dX, self.dW_qkv, self.dW_o = orc.layer_backward(f["X"], f["W_qkv"], f["W_o"], sh.H, sh.G,
+                                                                 sh.d_head, f["dY"])
+        self.dev = {k: to_dev(v) for k, v in self.bits.items()}
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return Ref(SHAPES["tiny"])
+
+
+def _guarded(shape, dtype, guard=4096):
+    """A tensor inside a larger buffer whose guard bands hold a sentinel."""
+    import torch
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * guard,), 0, dtype=dtype, device="cuda")
+    buf.view(torch.uint8 if dtype != torch.float32 else torch.int32).fill_(0x5A if dtype != torch.float32 else 0x5A5A5A5A)
+    return buf, buf[guard:guard + n].view(*shape), guard
+
+
+def _guard_ok(buf, guard, n):
+    import torch
+    raw = buf.view(torch.uint8)
+    per = buf.element_size()
+    head = raw[:guard * per]
+    tail = raw[(guard + n) * per:]
+    return bool((head == 0x5A).all()) and bool((tail == 0x5A).all())
+
+
+def _run(up, ref, U, C, sched, check_guards=False):
+    import torch
+    sh = ref.sh
+    s = up.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, U, C, sched)
+    d = ref.dev
+    bf, f32 = torch.bfloat16, torch.float32
+    outs = {}
+    if check_guards:
+        shapes = {"Y": ((sh.S, sh.d_model), bf), "O": ((sh.S, sh.H * sh.d_head), bf), "lse": ((sh.H, sh.S), f32),
+                  "dX": ((sh.S, sh.d_model), bf), "dW_qkv": ((sh.d_model, sh.qkv_cols), f32),
+                  "dW_o": ((sh.H * sh.d_head, sh.d_model), f32)}
+        for k, (shape, dt) in shapes.items():
+            outs[k] = _guarded(shape, dt)
+        extra = 1 << 20
+        wsf = torch.full((up.fwd_workspace_bytes(s) + extra,), 0xA5, dtype=torch.uint8, device="cuda")
+        wsb = torch.full((up.bwd_workspace_bytes(s) + extra,), 0xA5, dtype=torch.uint8, device="cuda")
+        Y, O, lse, stf = up.attn_fwd(d["X"], d["W_qkv"], d["W_o"], s, Y=outs["Y"][1], O_saved=outs["O"][1],
+                                     lse=outs["lse"][1], ws=wsf)
+        dX, dWqkv, dWo, stb = up.attn_bwd(d["X"], d["W_qkv"], d["W_o"], O, lse, d["dY"], s, dX=outs["dX"][1],
+                                          dW_qkv=outs["dW_qkv"][1], dW_o=outs["dW_o"][1], ws=wsb)
+        torch.cuda.synchronize()
+        for k, (buf, view, guard) in outs.items():
+            assert _guard_ok(buf, guard, view.numel()), f"guard band of {k} overwritten"
+        assert bool((wsf[-extra:] == 0xA5).all()) and bool((wsb[-extra:] == 0xA5).all()), "workspace overrun"
+    else:
+        Y, O, lse, stf = up.attn_fwd(d["X"], d["W_qkv"], d["W_o"], s)
+        dX, dWqkv, dWo, stb = up.attn_bwd(d["X"], d["W_qkv"], d["W_o"], O, lse, d["dY"], s)
+    up.sync_status()
+    return {"Y": f64_of(Y), "O": f64_of(O), "lse": f64_of(lse), "dX": f64_of(dX), "dW_qkv": f64_of(dWqkv),
+            "dW_o": f64_of(dWo), "stf": stf, "stb": stb}
+
+
+def _errors(ref, out):
+    return {"Y": rel(out["Y"], ref.Y), "O": rel(out["O"], ref.O), "dX": rel(out["dX"], ref.dX),
+            "dW_qkv": rel(out["dW_qkv"], ref.dW_qkv), "dW_o": rel(out["dW_o"], ref.dW_o),
+            "lse_abs": float(np.abs(out["lse"] - ref.lse).max())}
+
+
+def _tiny_cases():
+    H, G, S = 8, 2, 1024
+    for U in (1, 2, 4, 8):
+        for C in range(1, U + 1):
+            if U % C or S % C:
+                continue
+            for sched in (0, 1):
+                if sched == 1 and not (G % C == 0 or C % G == 0):
+                    continue
+                yield U, C, sched
+
+
+@pytest.mark.parametrize("U,C,sched", list(_tiny_cases()))
+def test_tiny_layer_matches_oracle_for_every_u(up, tiny, U, C, sched):
+    out = _run(up, tiny, U, C, sched, check_guards=(U == 2 and C == 2))
+    e = _errors(tiny, out)
+    assert max(e["Y"], e["O"], e["dX"], e["dW_qkv"], e["dW_o"]) <= TOL, e
+    assert e["lse_abs"] < 5e-3, e
+    st = out["stf"]
+    assert st["stages"] == 8 // U
+    sh = tiny.sh
+    if sched == 0:
+        assert st["arena_peak_bytes"] <= 12 * sh.S * U * sh.d_head + 1024
+    assert st["stage_closed_form_bytes"] == 12 * sh.S * U * sh.d_head
+
+
+def test_u_invariance_across_stages(up, tiny):
+    """Different U regroup the same sums: outputs agree with each other as
+    closely as each agrees with the oracle."""
+    outs = {U: _run(up, tiny, U, 2 if U >= 2 else 1, 0) for U in (2, 4, 8)}
+    for U in (2, 4):
+        for k in ("Y", "dX", "dW_qkv", "dW_o"):
+            assert rel(outs[U][k], outs[8][k]) <= TOL, (U, k)
+
+
+@pytest.mark.parametrize("sched", [0, 1])
+def test_llama_widths_4k(up, sched):
+    ref = Ref(SHAPES["llama3_8b_4k"])
+    out = _run(up, ref, 8, 8, sched)
+    e = _errors(ref, out)
+    assert max(e["Y"], e["O"], e["dX"], e["dW_qkv"], e["dW_o"]) <= TOL, e
+
+
+def test_llama_32k_sampled_rows(up):
+    """Full-size forward (the benchmarked launch configuration) against the
+    oracle on sampled query rows, each computed from its exact key prefix."""
+    import torch
+    sh = SHAPES["llama3_8b_32k"]
+    bits = layer_inputs(sh, 0)
+    dev = {k: to_dev(v) for k, v in bits.items() if k != "dY"}
+    for sched in (0, 1):
+        s = up.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, sh.U, sh.C, sched)
+        Y, O, lse, st = up.attn_fwd(dev["X"], dev["W_qkv"], dev["W_o"], s)
+        torch.cuda.synchronize()
+        up.sync_status()
+        rows = np.array([0, 1, 127, 128, 4095, 8191, 16384, 20000, 32766, 32767])
+        f = {k: bf16_bits_to_f64(bits[k]) for k in ("X", "W_qkv", "W_o")}
+        if sched == 0:
+            Yr, Or, lser = orc.layer_forward_rows(f["X"], f["W_qkv"], f["W_o"], sh.H, sh.G, sh.d_head, rows)
+        got = f64_of(Y[torch.as_tensor(rows, device="cuda")])
+        assert rel(got, Yr) <= TOL
+        assert np.abs(f64_of(lse)[:, rows] - lser).max() < 5e-3
