@@ -13,7 +13,8 @@
 //
 // head2seq can sum several source slots into one output head (the copies of
 // a KV head's gradient held by different ranks), in fp32, in the listed
-// order, then rounds once to bf16 (round to nearest even).
+// order starting from the first source, then rounds once to bf16 (round to
+// nearest even).  A single bf16 source is moved bit for bit.
 #include <algorithm>
 
 #include "ptx.cuh"
@@ -47,26 +48,35 @@ __global__ void head2seq_kernel(const Head2SeqDesc p) {
     const long long rest = g / vpr;
     const int t = static_cast<int>(rest % p.S);
     const int k = static_cast<int>(rest / p.S);
-    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int r = p.first[k]; r < p.first[k + 1]; ++r) {
+    uint4* out = reinterpret_cast<uint4*>(p.dst + t * p.ld_dst + static_cast<long long>(p.dst_head[k]) * p.D + v * 8);
+    const int r0 = p.first[k], r1 = p.first[k + 1];
+    if (!F32 && r1 - r0 == 1) {  // a plain move: copy the bits
+      *out = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.src) +
+                                             (static_cast<long long>(p.src_slot[r0]) * p.S + t) * p.D + v * 8);
+      continue;
+    }
+    float f[8];
+    for (int r = r0; r < r1; ++r) {
       const long long off = (static_cast<long long>(p.src_slot[r]) * p.S + t) * p.D + v * 8;
+      float x[8];
       if (F32) {
         const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(p.src) + off);
         const float4 a = s[0], b = s[1];
-        f[0] += a.x; f[1] += a.y; f[2] += a.z; f[3] += a.w;
-        f[4] += b.x; f[5] += b.y; f[6] += b.z; f[7] += b.w;
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
       } else {
         const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.src) + off);
         const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          f[2 * i] += bf16_lo(w[i]);
-          f[2 * i + 1] += bf16_hi(w[i]);
+          x[2 * i] = bf16_lo(w[i]);
+          x[2 * i + 1] = bf16_hi(w[i]);
         }
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = (r == r0) ? x[i] : f[i] + x[i];
     }
-    *reinterpret_cast<uint4*>(p.dst + t * p.ld_dst + static_cast<long long>(p.dst_head[k]) * p.D + v * 8) =
-        make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+    *out = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
   }
 }
 
