@@ -24,7 +24,7 @@ OK, EINVAL, ENOSPC, EUNSUPPORTED, ECUDA, ETIMEOUT = range(6)
 EXPORTS = (
     "upipe_fwd_workspace_bytes", "upipe_bwd_workspace_bytes", "upipe_attn_fwd", "upipe_attn_bwd",
     "upipe_layout_seq2head", "upipe_layout_head2seq", "upipe_schedule_table",
-    "upipe_attention_fwd", "upipe_attention_bwd", "upipe_gemm_bf16",
+    "upipe_attention_fwd", "upipe_attention_bwd", "upipe_attention_bwd_noalloc", "upipe_gemm_bf16",
     "upipe_sync_status", "upipe_status_str", "upipe_version", "upipe_profile_enable", "upipe_profile_read",
 )
 
@@ -70,6 +70,7 @@ def _sig(lib):
         "upipe_schedule_table": (I, [I, I, I, I, I, i32p]),
         "upipe_attention_fwd": (I, [P, P, P, I, I, I, I, i32p, P, P, P]),
         "upipe_attention_bwd": (I, [P, P, P, P, P, P, I, I, I, I, i32p, P, P, P, P, Z, P]),
+        "upipe_attention_bwd_noalloc": (I, [P, P, P, P, P, P, I, I, I, I, i32p, P, P, P, P]),
         "upipe_gemm_bf16": (I, [P, P, P, I, I, I, I, I, LL, LL, LL, I, P]),
         "upipe_sync_status": (I, [P]),
         "upipe_status_str": (ctypes.c_char_p, [I]),
@@ -250,6 +251,20 @@ def attention_bwd(Q, K, V, O, dO, lse, kv_of_q, stream=None):
         _ptr(Q, bf, "Q"), _ptr(K, bf, "K"), _ptr(V, bf, "V"), _ptr(O, bf, "O"), _ptr(dO, bf, "dO"),
         _ptr(lse, f32, "lse"), n_q, n_kv, S, d, _i32(kv_of_q), _ptr(dQ), _ptr(dK), _ptr(dV),
         _ptr(ws), ws.numel(), _stream(stream)))
+    return dQ, dK, dV
+
+
+def attention_bwd_noalloc(Q, K, V, O, dO, lse, kv_of_q, dQ, dK, dV, stream=None):
+    """``attention_bwd`` for callers that cannot allocate: no workspace, the
+    scratch is a fixed 8 MiB array inside the library (n_q * S <= 1,048,576).
+    Outputs are written into the caller's dQ, dK, dV."""
+    torch = _torch()
+    bf, f32 = torch.bfloat16, torch.float32
+    n_q, S, d = Q.shape
+    _check("upipe_attention_bwd_noalloc", lib().upipe_attention_bwd_noalloc(
+        _ptr(Q, bf, "Q"), _ptr(K, bf, "K"), _ptr(V, bf, "V"), _ptr(O, bf, "O"), _ptr(dO, bf, "dO"),
+        _ptr(lse, f32, "lse"), n_q, K.shape[0], S, d, _i32(kv_of_q), _ptr(dQ, f32, "dQ"), _ptr(dK, f32, "dK"),
+        _ptr(dV, f32, "dV"), _stream(stream)))
     return dQ, dK, dV
 
 

@@ -65,6 +65,8 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t o
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int* device_status_word() { return status_ptr(); }
+
 int num_sms() {
   if (!g_num_sms) {
     int dev = 0;

@@ -108,5 +108,7 @@ cudaError_t launch_bwd_prep(const BwdPrepDesc& p, cudaStream_t st);
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
                     uint32_t box_inner, uint32_t box_outer);
 int num_sms();
+// Device address of the status word bounded waits write (read by upipe_sync_status).
+int* device_status_word();
 
 }  // namespace upipe

@@ -174,6 +174,28 @@ int upipe_attention_bwd(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf
                         void* stream);
 
 /*
+ * upipe_attention_bwd for callers that cannot allocate device memory.  The
+ * pages have no counterpart: this is a deployment convenience, not part of the
+ * method.  Some callers own no allocator on their call path (an engine that
+ * reserves all device memory up front, a plugin inside another framework's
+ * operator that forbids allocations, code that must not call cudaMalloc
+ * because it synchronises the device), so this variant needs no `ws`: its
+ * 8*n_q*S bytes of scratch come from a fixed 8 MiB array compiled into the
+ * library, present on every GPU that loads it until the process exits.
+ *   Arguments, layouts and results: as upipe_attention_bwd, without ws.
+ *   Limit: 8*n_q*S <= 8 MiB (n_q*S <= 1,048,576), else UPIPE_ENOSPC before any launch.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any stream
+ *   capture begins.  All calls on a device share the array, which keeps the
+ *   last call's contents: calls whose work overlaps on the GPU race; calls
+ *   ordered on one stream do not.  Calls no cudaMalloc, cudaFree or allocating
+ *   library routine.
+ */
+int upipe_attention_bwd_noalloc(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf16* V, const upipe_bf16* O,
+                                const upipe_bf16* dO, const float* lse, int n_q, int n_kv, int S, int d_head,
+                                const int32_t* kv_of_q, float* dQ, float* dK, float* dV, void* stream);
+
+/*
  * The dense contraction behind the projections (Method steps (1) and the
  * output projection): D[M,N] = A[M,K] B[K,N], bf16 in, fp32 accumulate.
  *   A : device bf16, stored [M][K] (a_trans == 0) or [K][M] (a_trans == 1), row stride lda.
