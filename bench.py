@@ -168,6 +168,42 @@ def workload_config(args, sh):
                                   "GBs through HBM)"}
 
 
+def run_kernel_profile(args, sh):
+    """One stage's attention kernels in isolation (U query slots, in-order KV
+    copies), for ncu captures on small cases and quick kernel timing."""
+    import torch
+    import headwise_chunked_ulysses_gb300 as upipe
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(0)
+    n_q = n_kv = sh.U
+    shape = (n_q, sh.S, sh.d_head)
+    Q, K, V, dO = (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16) for _ in range(4))
+    kv = list(range(n_q))
+    O, lse = upipe.attention_fwd(Q, K, V, kv)
+    pairs = sh.S * (sh.S + 1) / 2
+    res = {}
+    for name, fn, flops in (("attn_fwd", lambda: upipe.attention_fwd(Q, K, V, kv, O=O, lse=lse),
+                             4 * sh.d_head * pairs * n_q),
+                            ("attn_bwd", lambda: upipe.attention_bwd(Q, K, V, O, dO, lse, kv),
+                             10 * sh.d_head * pairs * n_q)):
+        if args.profile_kernel not in (name, "all"):
+            continue
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.reps
+        res[name] = {"ms": ms, "tflops": flops / (ms / 1e3) / 1e12}
+    upipe.sync_status()
+    print(json.dumps({"profile_kernel": args.profile_kernel, "S": sh.S, "U": sh.U, "d_head": sh.d_head,
+                      "note": "bwd time includes its preprocessing kernel", "kernels": res}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -182,6 +218,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
     ap.add_argument("--ref-sample-tokens", type=int, default=2048)
+    ap.add_argument("--profile-kernel", default=None, choices=["attn_fwd", "attn_bwd", "all"],
+                    help="time one stage's attention kernels alone (no JSON bench line)")
+    ap.add_argument("--reps", type=int, default=5)
     args = ap.parse_args()
 
     from synthetic import SHAPES
@@ -192,6 +231,8 @@ def main():
         sh = sh.replace(S=args.S)
     if args.impl == "reference":
         return run_reference(args, sh)
+    if args.profile_kernel:
+        return run_kernel_profile(args, sh)
 
     rank, world, local = dist_env()
     import numpy as np
