@@ -204,6 +204,62 @@ def run_kernel_profile(args, sh):
     return 0
 
 
+def run_sweep(args):
+    """The other workloads: one JSON line each (tokens/s, TFLOP/s, stage-arena
+    bytes against the 12*S*U*d_head form, exchanged bytes).  Not the headline."""
+    import numpy as np
+    import torch
+    import headwise_chunked_ulysses_gb300 as upipe
+    from synthetic import SHAPES
+    dev = torch.device("cuda", 0)
+    pk = peaks()
+    cases = []
+    us = SHAPES["llama3_8b_256k_usweep"]
+    for U in (8, 16, 32):
+        cases.append(("llama3_8b_256k_usweep", us.replace(U=U), 0))
+    gq = SHAPES["llama3_8b_512k_gqa"]
+    cases += [("llama3_8b_512k_gqa", gq, 0), ("llama3_8b_512k_gqa", gq, 1)]
+    cases.append(("qwen3_32b_128k", SHAPES["qwen3_32b_128k"], 0))
+    if args.sweep_only:
+        cases = [c for c in cases if c[0] in args.sweep_only.split(",")]
+    for name, sh, sched in cases:
+        s = upipe.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, sh.U, sh.C, sched)
+        g = torch.Generator(device=dev).manual_seed(0)
+        w_std = 1.0 / np.sqrt(sh.d_model)
+
+        def randn(*shape, std=1.0):
+            return (torch.randn(*shape, generator=g, device=dev) * std).to(torch.bfloat16)
+        X, dY = randn(sh.S, sh.d_model), randn(sh.S, sh.d_model)
+        Wqkv, Wo = randn(sh.d_model, sh.qkv_cols, std=w_std), randn(sh.H * sh.d_head, sh.d_model, std=w_std)
+        wsf = torch.empty(upipe.fwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
+        wsb = torch.empty(upipe.bwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
+        Y, O, lse, _ = upipe.attn_fwd(X, Wqkv, Wo, s, ws=wsf)
+        dX, dWqkv, dWo, _ = upipe.attn_bwd(X, Wqkv, Wo, O, lse, dY, s, ws=wsb)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.sweep_steps):
+            _, _, _, stf = upipe.attn_fwd(X, Wqkv, Wo, s, Y=Y, O_saved=O, lse=lse, ws=wsf)
+            _, _, _, stb = upipe.attn_bwd(X, Wqkv, Wo, O, lse, dY, s, dX=dX, dW_qkv=dWqkv, dW_o=dWo, ws=wsb)
+        e1.record()
+        torch.cuda.synchronize()
+        upipe.sync_status()
+        ms = e0.elapsed_time(e1) / args.sweep_steps
+        tf = model_flops_step(sh) / (ms / 1e3) / 1e12
+        print(json.dumps({
+            "sweep": name, "S": sh.S, "U": sh.U, "C": sh.C, "H": sh.H, "G": sh.G, "d_model": sh.d_model,
+            "schedule": "gqa_out_of_order" if sched else "in_order", "ms_per_step": ms,
+            "tokens_per_s": sh.S / (ms / 1e3), "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops_sustained"],
+            "stage_arena_fwd_bytes": stf["arena_peak_bytes"], "stage_arena_bwd_bytes": stb["arena_peak_bytes"],
+            "closed_form_12SUd": stf["stage_closed_form_bytes"],
+            "ulysses_form_12SHd": 12 * sh.S * sh.H * sh.d_head,
+            "permute_bytes_fwd": stf["permute_bytes"], "permute_bytes_bwd": stb["permute_bytes"],
+            "persistent_bytes": stf["persistent_bytes"], "steps": args.sweep_steps}), flush=True)
+        del X, dY, Wqkv, Wo, wsf, wsb, Y, O, lse, dX, dWqkv, dWo
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -221,6 +277,9 @@ def main():
     ap.add_argument("--profile-kernel", default=None, choices=["attn_fwd", "attn_bwd", "all"],
                     help="time one stage's attention kernels alone (no JSON bench line)")
     ap.add_argument("--reps", type=int, default=5)
+    ap.add_argument("--sweep", action="store_true", help="report the other workloads (U sweep, GQA schedule, Qwen)")
+    ap.add_argument("--sweep-only", default=None, help="comma-separated workload names for --sweep")
+    ap.add_argument("--sweep-steps", type=int, default=1)
     args = ap.parse_args()
 
     from synthetic import SHAPES
@@ -233,6 +292,8 @@ def main():
         return run_reference(args, sh)
     if args.profile_kernel:
         return run_kernel_profile(args, sh)
+    if args.sweep:
+        return run_sweep(args)
 
     rank, world, local = dist_env()
     import numpy as np

@@ -10,11 +10,19 @@
 //
 // One CTA per (KV slot, 128-row KV block).  It walks every query slot mapped
 // to its KV slot and every query block at or after its KV block, so the GQA
-// reduction of dK/dV happens in TMEM with no atomics.  Per step:
+// reduction of dK/dV happens in TMEM with no atomics.  Per step i:
 //   S^T = K Q^T, dP^T = V dO^T  (tensor cores -> TMEM)
-//   warps 4..7 (one KV row each): P^T -> smem, then dS^T -> smem (same buffer)
-//   dV += P^T dO, dK += dS^T Q, dQ = dS K  (tensor cores; dQ reuses dP's TMEM)
-//   warps 8..11 (one query row each): dQ -> fp32 vector atomics into global.
+//   warps 4..11, two per TMEM lane quarter, each thread owning half of one
+//     KV row (64 query columns): P^T as bf16 back into S^T's TMEM columns,
+//     then dS^T = P^T * (dP^T - D) as bf16 into shared memory
+//   dV += P^T dO (A operand read from TMEM), dK += dS^T Q, dQ = dS K
+//     (tensor cores; dQ reuses dP's TMEM columns)
+//   the same warps, between P_{i+1} and dS_{i+1}, add dQ_i (half a query row
+//   per thread) into global memory with fp32 vector atomics.
+// MMA issue order dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}: the next scores are
+// computed while the softmax warps build dS_i.  The tensor pipe executes one
+// CTA's MMAs in issue order, so S_{i+1} overwrites P^T_i only after dV_i has
+// read it.
 #include <cmath>
 
 #include "ptx.cuh"
@@ -31,6 +39,7 @@ struct BwdArgs {
   int S, n_qslots, n_kvslots, q_blocks;
   float scale_log2, scale;
   int accumulate_kv;
+  int dq_tiled;
   uint16_t kv_slot[kMaxSlots];
   const float* lse2;
   const float* Dsum;
@@ -47,12 +56,13 @@ struct BwdCfg {
   static constexpr int V_OFF = TILE;
   static constexpr int Q_OFF = 2 * TILE;    // 2 stages
   static constexpr int DO_OFF = 4 * TILE;   // 2 stages
-  static constexpr int PDS_OFF = 6 * TILE;  // 128 x 128 bf16, P^T then dS^T
-  static constexpr int LSE_OFF = PDS_OFF + BKV * BQ * 2;  // 2 stages x 128 fp32
+  static constexpr int DS_TILE_OFF = 6 * TILE;  // dS^T, 128 x 128 bf16
+  static constexpr int LSE_OFF = DS_TILE_OFF + BKV * BQ * 2;  // 2 stages x 128 fp32
   static constexpr int DS_OFF = LSE_OFF + 2 * BQ * 4;     // 2 stages x 128 fp32
   static constexpr int BAR_OFF = DS_OFF + 2 * BQ * 4;
   static constexpr int SMEM = BAR_OFF + 256;
-  // TMEM: S^T [0,128)  dP^T / dQ [128,256)  dV [256,256+D)  dK [256+D,256+2D)
+  // TMEM: S^T [0,128) (then P^T as bf16 pairs in [0,32) and [64,96))
+  //       dP^T / dQ [128,256)  dV [256,256+D)  dK [256+D,256+2D)
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
 };
@@ -82,7 +92,6 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* s_full = bars + 5;
   uint64_t* dp_full = bars + 6;
   uint64_t* p_ready = bars + 7;
-  uint64_t* p_consumed = bars + 8;
   uint64_t* ds_ready = bars + 9;
   uint64_t* ds_consumed = bars + 10;
   uint64_t* dq_full = bars + 11;
@@ -111,12 +120,11 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_ready, 128);
-    mbar_init(p_consumed, 1);
-    mbar_init(ds_ready, 128);
+    mbar_init(p_ready, 256);
+    mbar_init(ds_ready, 256);
     mbar_init(ds_consumed, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_drained, 128);
+    mbar_init(dq_drained, 256);
     mbar_init(kv_done, 1);
     *abort_flag = aligned ? 0 : 1;
     if (!aligned && a.status) atomicCAS(a.status, 0, kDevBadSmem);
@@ -130,7 +138,6 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
   if (aligned && n_items > 0) {
     if (warp == 0 && lane == 0) {
       // ---------------- TMA producer ----------------
@@ -168,7 +175,7 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t ID_Q = idesc_bf16(BQ, D, true, true);      // dQ
       const uint32_t sK = smem_u32(smem + C::K_OFF);
       const uint32_t sV = smem_u32(smem + C::V_OFF);
-      const uint32_t sPdS = smem_u32(smem + C::PDS_OFF);
+      const uint32_t sDS = smem_u32(smem + C::DS_TILE_OFF);
       auto sQ = [&](int st) { return smem_u32(smem + C::Q_OFF + st * C::TILE); };
       auto sdO = [&](int st) { return smem_u32(smem + C::DO_OFF + st * C::TILE); };
       auto qk_mma = [&](uint32_t d_tmem, uint32_t sA, uint32_t sB) {
@@ -188,17 +195,15 @@ __global__ void __launch_bounds__(384, 1)
       }
       for (int i = 0; ok && i < n_items; ++i) {
         const int st = i & 1;
-        // dV += P^T dO
+        // dV += P^T dO, P^T read from TMEM (16 bf16 of K per 8 columns): query
+        // columns [0,64) at S^T columns [0,32), [64,128) at [64,96)
         if (!mbar_wait(p_ready, i & 1, w, 43)) break;
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < BQ / 16; ++k) {
-          const uint32_t poff = (k >> 2) * CH + (k & 3) * 32;
-          mma_ss(tmem + C::T_DV, sdesc_kmajor(sPdS + poff), sdesc_mnmajor(sdO(st) + k * 2048, CH), ID_KV,
-                 (i | k) != 0);
-        }
-        mma_commit(p_consumed);
-        // next S^T (the softmax warps have read this one)
+        for (int k = 0; k < BQ / 16; ++k)
+          mma_ts(tmem + C::T_DV, tmem + C::T_S + (k >> 2) * 64 + (k & 3) * 8, sdesc_mnmajor(sdO(st) + k * 2048, CH),
+                 ID_KV, (i | k) != 0);
+        // next S^T: issued after dV_i, so it overwrites P^T_i only once dV_i has read it
         if (i + 1 < n_items) {
           if (!mbar_wait(&qdo_full[st ^ 1], ((i + 1) >> 1) & 1, w, 44)) break;
           tc_fence_after();
@@ -211,12 +216,12 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k) {
           const uint32_t poff = (k >> 2) * CH + (k & 3) * 32;
-          mma_ss(tmem + C::T_DK, sdesc_kmajor(sPdS + poff), sdesc_mnmajor(sQ(st) + k * 2048, CH), ID_KV,
+          mma_ss(tmem + C::T_DK, sdesc_kmajor(sDS + poff), sdesc_mnmajor(sQ(st) + k * 2048, CH), ID_KV,
                  (i | k) != 0);
         }
 #pragma unroll
         for (int k = 0; k < BKV / 16; ++k)
-          mma_ss(tmem + C::T_DP, sdesc_mnmajor(sPdS + k * 2048, CH), sdesc_mnmajor(sK + k * 2048, CH), ID_Q, k > 0);
+          mma_ss(tmem + C::T_DP, sdesc_mnmajor(sDS + k * 2048, CH), sdesc_mnmajor(sK + k * 2048, CH), ID_Q, k > 0);
         mma_commit(ds_consumed);
         mma_commit(dq_full);
         mma_commit(&qdo_empty[st]);
@@ -229,63 +234,86 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if (ok) mma_commit(kv_done);
-    } else if (warp >= 4 && warp < 8) {
-      // ---------------- P^T and dS^T: one KV row per thread ----------------
+    } else if (warp >= 4) {
+      // ---------------- softmax, dS and dQ: half a row per thread ----------------
       const int q4 = warp & 3;
-      const int row = q4 * 32 + lane;
+      const int half = (warp - 4) >> 2;  // 0: columns [0,64), 1: [64,128)
+      const int row = q4 * 32 + lane;    // TMEM lane = KV row (S^T, dP^T) or query row (dQ)
       const int kv_idx = kvb * BKV + row;
       const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-      const uint32_t sPdS = smem_u32(smem + C::PDS_OFF);
+      const uint32_t sDS = smem_u32(smem + C::DS_TILE_OFF);
       const float sl2 = a.scale_log2;
-      ItemCursor cur;
-      cur.kvb = kvb;
-      cur.q_blocks = a.q_blocks;
+      ItemCursor cur, prev;
+      cur.kvb = prev.kvb = kvb;
+      cur.q_blocks = prev.q_blocks = a.q_blocks;
+      // dQ of the previous step (query row `row`, this thread's half of d) into global
+      auto drain_dq = [&](int i) -> bool {
+        if (!mbar_wait_warp(dq_full, i & 1, w, 53)) return false;
+        tc_fence_after();
+        const long long qrow = static_cast<long long>(prev.qs) * a.S + prev.qb * BQ + row;
+        // address of the 4 columns starting at column 4*g of query row qrow
+        auto col4 = [&](int g) -> float* {
+          return a.dq_tiled ? a.dQacc + ((qrow >> 5) * (D / 4) + g) * 128 + (qrow & 31) * 4
+                            : a.dQacc + qrow * D + 4 * g;
+        };
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + C::T_DP + half * (D / 2) + c * 32, v);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            red_add_v4(col4((half * (D / 2) + c * 32) / 4 + e), __uint_as_float(v[4 * e]) * a.scale,
+                       __uint_as_float(v[4 * e + 1]) * a.scale, __uint_as_float(v[4 * e + 2]) * a.scale,
+                       __uint_as_float(v[4 * e + 3]) * a.scale);
+        }
+        tc_fence_before();
+        mbar_arrive(dq_drained);
+        return true;
+      };
       bool ok = true;
-      for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
+      int i = 0;
+      for (; i < n_items && cur.next(a, kvs); ++i) {
         const int st = i & 1;
         const bool diag = (cur.qb == kvb);
         if (!mbar_wait_warp(s_full, i & 1, w, 47)) { ok = false; break; }
         if (!mbar_wait_warp(&qdo_full[st], (i >> 1) & 1, w, 48)) { ok = false; break; }
         tc_fence_after();
-        const float* lse = s_lse + st * BQ;
-        const float* Dv = s_D + st * BQ;
-        uint32_t pk[BQ / 2];
+        const float* lse = s_lse + st * BQ + half * 64;
+        const float* Dv = s_D + st * BQ + half * 64;
+        uint32_t pk[32];  // P^T of query columns [64*half, 64*half+64) as bf16 pairs
 #pragma unroll
-        for (int c = 0; c < BQ / 32; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_off + C::T_S + c * 32, v);
+          tmem_ld32(tmem + lane_off + C::T_S + half * 64 + c * 32, v);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const int q0 = c * 32 + e;
+            const int q0 = c * 32 + e;  // within this half
             float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, -lse[q0]));
             float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -lse[q0 + 1]));
             if (diag) {
-              if (q0 < row) p0 = 0.f;
-              if (q0 + 1 < row) p1 = 0.f;
+              if (half * 64 + q0 < row) p0 = 0.f;
+              if (half * 64 + q0 + 1 < row) p1 = 0.f;
             }
-            pk[(c * 32 + e) >> 1] = pack_bf16(p0, p1);
+            pk[q0 >> 1] = pack_bf16(p0, p1);
           }
         }
-        // the shared P/dS buffer is free once the previous step's dK and dQ MMAs are done
-        if (i > 0 && !mbar_wait_warp(ds_consumed, (i - 1) & 1, w, 49)) { ok = false; break; }
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int piece = 0; piece < 8; ++piece) {
-            const int b = c * 32 + piece * 4;
-            st_shared_v4(sPdS + c * CH + row * 128 + ((piece ^ (row & 7)) << 4), pk[b], pk[b + 1], pk[b + 2],
-                         pk[b + 3]);
-          }
-        fence_proxy_async_smem();
+        // P^T (bf16 pairs) into the first 32 columns of this half's own S^T
+        // columns, which only this thread has read
+        tmem_st32(tmem + lane_off + C::T_S + half * 64, pk);
         tc_fence_before();
         mbar_arrive(p_ready);
+        // dQ of the previous step, while the tensor cores run dV_i and S_{i+1}
+        if (i > 0) {
+          if (!drain_dq(i - 1)) { ok = false; break; }
+        }
+        prev = cur;
         // dS^T = P^T * (dP^T - D)
         if (!mbar_wait_warp(dp_full, i & 1, w, 50)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < BQ / 32; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_off + C::T_DP + c * 32, v);
+          tmem_ld32(tmem + lane_off + C::T_DP + half * 64 + c * 32, v);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int q0 = c * 32 + e;
@@ -295,31 +323,28 @@ __global__ void __launch_bounds__(384, 1)
             pk[q0 >> 1] = pack_bf16(d0, d1);
           }
         }
-        tc_fence_before();
-        if (!mbar_wait_warp(p_consumed, i & 1, w, 51)) { ok = false; break; }
+        // the dS^T buffer is free once the previous step's dK and dQ MMAs are done
+        if (i > 0 && !mbar_wait_warp(ds_consumed, (i - 1) & 1, w, 49)) { ok = false; break; }
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int piece = 0; piece < 8; ++piece) {
-            const int b = c * 32 + piece * 4;
-            st_shared_v4(sPdS + c * CH + row * 128 + ((piece ^ (row & 7)) << 4), pk[b], pk[b + 1], pk[b + 2],
-                         pk[b + 3]);
-          }
+        for (int piece = 0; piece < 8; ++piece)
+          st_shared_v4(sDS + half * CH + row * 128 + ((piece ^ (row & 7)) << 4), pk[piece * 4], pk[piece * 4 + 1],
+                       pk[piece * 4 + 2], pk[piece * 4 + 3]);
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(ds_ready);
       }
-      // dK, dV epilogue
+      if (ok && i > 0) ok = drain_dq(i - 1);
+      // dK, dV epilogue: this thread's half of the d columns of KV row `row`
       if (ok && mbar_wait_warp(kv_done, 0, w, 52)) {
         tc_fence_after();
-        const long long base = (static_cast<long long>(kvs) * a.S + kv_idx) * D;
+        const long long base = (static_cast<long long>(kvs) * a.S + kv_idx) * D + half * (D / 2);
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
           float* dst = (which == 0 ? a.dV : a.dK) + base;
           const float mul = which == 0 ? 1.f : a.scale;
-          const uint32_t col = which == 0 ? C::T_DV : C::T_DK;
+          const uint32_t col = (which == 0 ? C::T_DV : C::T_DK) + half * (D / 2);
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < D / 64; ++c) {
             uint32_t v[32];
             tmem_ld32(tmem + lane_off + col + c * 32, v);
             float4* o = reinterpret_cast<float4*>(dst + c * 32);
@@ -336,37 +361,13 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-    } else if (warp >= 8) {
-      // ---------------- dQ drain: one query row per thread ----------------
-      const int q4 = warp & 3;
-      const int row = q4 * 32 + lane;
-      const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-      ItemCursor cur;
-      cur.kvb = kvb;
-      cur.q_blocks = a.q_blocks;
-      for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
-        if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
-        tc_fence_after();
-        float* dst = a.dQacc + (static_cast<long long>(cur.qs) * a.S + cur.qb * BQ + row) * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + C::T_DP + c * 32, v);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            red_add_v4(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]) * a.scale,
-                       __uint_as_float(v[4 * e + 1]) * a.scale, __uint_as_float(v[4 * e + 2]) * a.scale,
-                       __uint_as_float(v[4 * e + 3]) * a.scale);
-        }
-        tc_fence_before();
-        mbar_arrive(dq_drained);
-      }
     }
-  } else if (aligned && n_items == 0 && !a.accumulate_kv && warp >= 4 && warp < 8) {
+  } else if (aligned && n_items == 0 && !a.accumulate_kv && warp >= 4) {
     // a KV slot no query head uses in this launch: its gradient is zero
     const int row = (warp & 3) * 32 + lane;
-    const long long base = (static_cast<long long>(kvs) * a.S + kvb * BKV + row) * D;
-    for (int c = 0; c < D; c += 4) {
+    const int half = (warp - 4) >> 2;
+    const long long base = (static_cast<long long>(kvs) * a.S + kvb * BKV + row) * D + half * (D / 2);
+    for (int c = 0; c < D / 2; c += 4) {
       *reinterpret_cast<float4*>(a.dK + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
       *reinterpret_cast<float4*>(a.dV + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -411,6 +412,32 @@ __global__ void bwd_prep_kernel(const BwdPrepDesc p) {
   }
 }
 
+// Tiled fp32 dQ -> bf16 rows of the sequence layout, through shared memory:
+// one block per (32-token group, slot); reads are 512-byte runs, writes are
+// whole d-wide row segments.
+__global__ void __launch_bounds__(256) dq_tiled_to_seq_kernel(const DqTiledDesc p) {
+  __shared__ float tile[32][128 + 1];
+  const int groups = p.S / 32;
+  const int g = static_cast<int>(blockIdx.x) % groups;
+  const int k = static_cast<int>(blockIdx.x) / groups;
+  const int quads = p.D / 4;
+  const float* src = p.src + (static_cast<long long>(k) * groups + g) * quads * 128;
+  for (int idx = threadIdx.x; idx < 32 * quads; idx += blockDim.x) {
+    const int q = idx / 32, r = idx % 32;
+    const float4 x = *reinterpret_cast<const float4*>(src + q * 128 + r * 4);
+    tile[r][4 * q] = x.x; tile[r][4 * q + 1] = x.y; tile[r][4 * q + 2] = x.z; tile[r][4 * q + 3] = x.w;
+  }
+  __syncthreads();
+  const int vpr = p.D / 8;
+  for (int idx = threadIdx.x; idx < 32 * vpr; idx += blockDim.x) {
+    const int r = idx / vpr, v = idx % vpr;
+    const float* f = &tile[r][8 * v];
+    uint16_t* out = p.dst + (static_cast<long long>(g) * 32 + r) * p.ld_dst + static_cast<long long>(p.dst_head[k]) * p.D + 8 * v;
+    *reinterpret_cast<uint4*>(out) = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                                                pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+  }
+}
+
 template <int D>
 cudaError_t run_bwd(const CUtensorMap* tm, const BwdArgs& args, cudaStream_t st) {
   auto kern = attn_bwd_kernel<D>;
@@ -436,6 +463,12 @@ cudaError_t launch_bwd_prep(const BwdPrepDesc& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_dq_tiled_to_seq(const DqTiledDesc& p, cudaStream_t st) {
+  if ((p.D != 64 && p.D != 128) || p.S % 32 || p.n_slots <= 0 || p.n_slots > kMaxSlots) return cudaErrorInvalidValue;
+  dq_tiled_to_seq_kernel<<<(p.S / 32) * p.n_slots, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) {
   if ((d.D != 64 && d.D != 128) || d.S % 128 || d.n_qslots <= 0 || d.n_qslots > kMaxSlots ||
       d.n_kvslots <= 0)
@@ -453,6 +486,7 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) 
   a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.D)));
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.D)));
   a.accumulate_kv = d.accumulate_kv;
+  a.dq_tiled = d.dq_tiled;
   for (int i = 0; i < d.n_qslots; ++i) a.kv_slot[i] = d.kv_slot[i];
   a.lse2 = d.lse2;
   a.Dsum = d.Dsum;

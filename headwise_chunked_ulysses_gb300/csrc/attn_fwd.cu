@@ -5,16 +5,21 @@
 // log-sum-exp of every row saved for the backward pass.  Query slots map to
 // KV slots through a table, so grouped-query heads read their shared K/V.
 //
-// One CTA per (query slot, 128-row query block); blocks with the longest
-// causal rows are scheduled first.  Warp 0 streams K/V blocks of 128 rows by
-// TMA into a two-deep ring; warp 1 issues S = Q K^T (M=N=128) into one of two
-// TMEM score buffers while the softmax warps (4..7, one query row per
-// thread) turn the other into P (bf16, written to shared memory in the MMA's
-// 128-byte-swizzled K-major layout) and then O += P V accumulates in TMEM.
-// The online softmax keeps a per-row reference maximum and rescales the TMEM
-// accumulator only when the running maximum grows by more than 2^8, so the
-// rescale is rare and exact (the same reference enters numerator and
-// denominator).
+// One CTA per (query slot, 256 query rows) = two 128-row query tiles A and B
+// that take turns on the tensor cores; CTAs with the longest causal rows are
+// scheduled first.  TMEM (512 columns): S_A, S_B (128 fp32 columns each) and
+// O_A, O_B (d columns each).  Warp 0 streams 128-row K/V blocks by TMA into a
+// two-deep ring shared by both tiles; warp 1 issues, per KV block j,
+//   S_A(j) = Q_A K_j^T, S_B(j), then O_A += P_A(j) V_j, S_A(j+1), O_B += ...
+// Warps 4..7 (tile A) and 8..11 (tile B) own one query row per thread: they
+// read the row of S from TMEM, keep a per-row reference maximum (rescaling the
+// TMEM accumulator O only when the running maximum grows by more than 2^8,
+// which is exact since the same reference enters numerator and denominator),
+// and write P as bf16 pairs back into the first 64 columns of their S, where
+// the P V MMA reads its A operand.  The tensor pipe runs one CTA's MMAs in
+// issue order, so when S_T(j) is complete, O_T += P_T(j-1) V_{j-1} is complete
+// too: O is stable while the softmax warps rescale it, and P_T(j-1) has been
+// consumed before S_T(j) overwrites it.
 #include <cmath>
 
 #include "ptx.cuh"
@@ -23,13 +28,13 @@
 namespace upipe {
 namespace {
 
-constexpr int BQ = 128;   // query rows per CTA
-constexpr int BKV = 128;  // key rows per block
-constexpr int CH = 128 * 128;  // one 64-column chunk of a 128-row tile (bytes)
+constexpr int BQ = 128;        // query rows per tile (two tiles per CTA)
+constexpr int BKV = 128;       // key rows per block
+constexpr int CH = 128 * 128;  // one 64-column chunk of a 128-row bf16 tile (bytes)
 constexpr float kRescaleLog2 = 8.0f;
 
 struct FwdArgs {
-  int S, n_qslots, q_blocks;
+  int S, n_qslots, q_blocks, q_pairs;
   float scale_log2;
   uint16_t kv_slot[kMaxSlots];
   uint16_t lse_row[kMaxSlots];
@@ -41,17 +46,20 @@ struct FwdArgs {
 template <int D>
 struct FwdCfg {
   static constexpr int TILE = BQ * D * 2;
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = TILE;          // 2 stages
-  static constexpr int V_OFF = 3 * TILE;      // 2 stages
-  static constexpr int P_OFF = 5 * TILE;      // 128 x 128 bf16
-  static constexpr int BAR_OFF = P_OFF + BQ * BKV * 2;
+  static constexpr int QA_OFF = 0;
+  static constexpr int QB_OFF = TILE;
+  static constexpr int K_OFF = 2 * TILE;  // 2 stages
+  static constexpr int V_OFF = 4 * TILE;  // 2 stages
+  static constexpr int BAR_OFF = 6 * TILE;
   static constexpr int SMEM = BAR_OFF + 256;
-  static constexpr uint32_t TMEM_COLS = 512;  // S0 [0,128) S1 [128,256) O [256,256+D)
+  static constexpr uint32_t TMEM_COLS = 512;
+  // TMEM columns: S of tile t at t*128, O of tile t at 256 + t*D
+  static __device__ __forceinline__ uint32_t t_s(int tile) { return static_cast<uint32_t>(tile) * 128u; }
+  static __device__ __forceinline__ uint32_t t_o(int tile) { return 256u + static_cast<uint32_t>(tile) * D; }
 };
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdArgs a) {
   using C = FwdCfg<D>;
@@ -61,20 +69,24 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* k_full = bars + 1;    // [2]
   uint64_t* v_full = bars + 3;    // [2]
   uint64_t* kv_empty = bars + 5;  // [2]
-  uint64_t* s_full = bars + 7;    // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* pv_done = bars + 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* s_full = bars + 7;    // [2] per tile
+  uint64_t* p_ready = bars + 9;   // [2] per tile
+  uint64_t* o_done = bars + 11;   // [2] per tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Watch w{abort_flag, a.status};
   const bool aligned = (smem_u32(smem) & 1023u) == 0;
 
-  const int qb = a.q_blocks - 1 - static_cast<int>(blockIdx.x) / a.n_qslots;
+  // longest causal rows first: pair index t covers query blocks 2t and 2t+1
+  const int t = a.q_pairs - 1 - static_cast<int>(blockIdx.x) / a.n_qslots;
   const int slot = static_cast<int>(blockIdx.x) % a.n_qslots;
   const int kvs = a.kv_slot[slot];
-  const int n_kv = qb + 1;
+  const int qb0 = 2 * t, qb1 = 2 * t + 1;
+  const bool has_b = qb1 < a.q_blocks;
+  const int n_kv0 = qb0 + 1, n_kv1 = has_b ? qb1 + 1 : 0;
+  const int n_blocks = has_b ? n_kv1 : n_kv0;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -83,9 +95,9 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&kv_empty[s], 1);
       mbar_init(&s_full[s], 1);
+      mbar_init(&p_ready[s], 128);
+      mbar_init(&o_done[s], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
     *abort_flag = aligned ? 0 : 1;
     if (!aligned && a.status) atomicCAS(a.status, 0, kDevBadSmem);
     fence_mbar_init();
@@ -105,11 +117,13 @@ __global__ void __launch_bounds__(256, 1)
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
-      mbar_arrive_expect_tx(q_full, C::TILE);
+      mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::TILE);
+      for (int tile = 0; tile < (has_b ? 2 : 1); ++tile)
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_2d(smem + C::Q_OFF + c * CH, &tmQ, q_full, c * 64, slot * a.S + qb * BQ);
-      for (int j = 0; j < n_kv; ++j) {
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(smem + (tile ? C::QB_OFF : C::QA_OFF) + c * CH, &tmQ, q_full, c * 64,
+                      slot * a.S + (tile ? qb1 : qb0) * BQ);
+      for (int j = 0; j < n_blocks; ++j) {
         const int s = j & 1;
         if (!mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1, w, 20)) break;
         const int row = kvs * a.S + j * BKV;
@@ -126,10 +140,9 @@ __global__ void __launch_bounds__(256, 1)
       // ---------------- MMA issuer ----------------
       constexpr uint32_t ID_S = idesc_bf16(BQ, BKV, false, false);
       constexpr uint32_t ID_O = idesc_bf16(BQ, D, false, true);
-      const uint32_t sQ = smem_u32(smem + C::Q_OFF);
-      const uint32_t sP = smem_u32(smem + C::P_OFF);
+      const uint32_t sQ[2] = {smem_u32(smem + C::QA_OFF), smem_u32(smem + C::QB_OFF)};
       bool ok = mbar_wait(q_full, 0, w, 21);
-      auto issue_s = [&](int j) -> bool {
+      auto issue_s = [&](int tile, int j) -> bool {
         const int s = j & 1;
         if (!mbar_wait(&k_full[s], (j >> 1) & 1, w, 22)) return false;
         tc_fence_after();
@@ -137,123 +150,135 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * CH + (k & 3) * 32;
-          mma_ss(tmem + s * BKV, sdesc_kmajor(sQ + off), sdesc_kmajor(sK + off), ID_S, k > 0);
+          mma_ss(tmem + C::t_s(tile), sdesc_kmajor(sQ[tile] + off), sdesc_kmajor(sK + off), ID_S, k > 0);
         }
-        mma_commit(&s_full[s]);
+        mma_commit(&s_full[tile]);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n_kv; ++j) {
+      auto issue_pv = [&](int tile, int j) -> bool {
         const int s = j & 1;
-        if (j + 1 < n_kv && !issue_s(j + 1)) break;
-        if (!mbar_wait(p_full, j & 1, w, 23)) break;
-        if (!mbar_wait(&v_full[s], (j >> 1) & 1, w, 24)) break;
+        if (!mbar_wait(&p_ready[tile], j & 1, w, 23)) return false;
+        if (!mbar_wait(&v_full[s], (j >> 1) & 1, w, 24)) return false;
         tc_fence_after();
         const uint32_t sV = smem_u32(smem + C::V_OFF + s * C::TILE);
 #pragma unroll
-        for (int k = 0; k < BKV / 16; ++k) {
-          const uint32_t poff = (k >> 2) * CH + (k & 3) * 32;
-          mma_ss(tmem + 256, sdesc_kmajor(sP + poff), sdesc_mnmajor(sV + k * 2048, CH), ID_O, (j | k) != 0);
+        for (int k = 0; k < BKV / 16; ++k)
+          mma_ts(tmem + C::t_o(tile), tmem + C::t_s(tile) + k * 8, sdesc_mnmajor(sV + k * 2048, CH), ID_O,
+                 (j | k) != 0);
+        return true;
+      };
+      if (ok) ok = issue_s(0, 0);
+      if (ok && has_b) ok = issue_s(1, 0);
+      for (int j = 0; ok && j < n_blocks; ++j) {
+        const int s = j & 1;
+        if (j < n_kv0) {
+          if (!issue_pv(0, j)) break;
+          if (j + 1 < n_kv0) {
+            if (!issue_s(0, j + 1)) break;
+          } else {
+            mma_commit(&o_done[0]);
+          }
         }
-        mma_commit(pv_done);
+        if (has_b) {
+          if (!issue_pv(1, j)) break;
+          if (j + 1 < n_kv1) {
+            if (!issue_s(1, j + 1)) break;
+          } else {
+            mma_commit(&o_done[1]);
+          }
+        }
         mma_commit(&kv_empty[s]);
       }
     } else if (warp >= 4) {
-      // ---------------- softmax: one query row per thread ----------------
-      const int q4 = warp & 3;
-      const int row = q4 * 32 + lane;
-      const int qi = qb * BQ + row;
-      const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-      const float sl2 = a.scale_log2;
-      float m_run = -INFINITY, l_run = 0.f;
-      bool ok = true;
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait_warp(&s_full[s], (j >> 1) & 1, w, 25)) { ok = false; break; }
-        tc_fence_after();
-        float x[BKV];
-#pragma unroll
-        for (int c = 0; c < BKV / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + s * BKV + c * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(v[i]);
-        }
-        if (j == n_kv - 1) {
-          const int lim = qi - j * BKV;  // keys with column index > lim are in the future
-#pragma unroll
-          for (int i = 0; i < BKV; ++i)
-            if (i > lim) x[i] = -INFINITY;
-        }
-        float mx = x[0];
-#pragma unroll
-        for (int i = 1; i < BKV; ++i) mx = fmaxf(mx, x[i]);
-        const float m_new = fmaxf(m_run, mx * sl2);
-        float alpha = 1.f;
-        bool resc = false;
-        if (m_new > m_run + kRescaleLog2) {
-          alpha = ex2(m_run - m_new);
-          m_run = m_new;
-          resc = true;
-        }
-        uint32_t pk[BKV / 2];
-        float rs = 0.f;
-#pragma unroll
-        for (int i = 0; i < BKV / 2; ++i) {
-          const float p0 = ex2(fmaf(x[2 * i], sl2, -m_run));
-          const float p1 = ex2(fmaf(x[2 * i + 1], sl2, -m_run));
-          rs += p0 + p1;
-          pk[i] = pack_bf16(p0, p1);
-        }
-        l_run = l_run * alpha + rs;
-        if (j > 0) {
-          // P buffer and the O accumulator are free once P_{j-1} V_{j-1} is done.
-          if (!mbar_wait_warp(pv_done, (j - 1) & 1, w, 26)) { ok = false; break; }
+      // ---------------- softmax: one query row of one tile per thread ----------------
+      const int tile = (warp - 4) >> 2;
+      if (tile == 0 || has_b) {
+        const int q4 = warp & 3;
+        const int row = q4 * 32 + lane;
+        const int qi = (tile ? qb1 : qb0) * BQ + row;
+        const int nkv = tile ? n_kv1 : n_kv0;
+        const uint32_t t_s = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + C::t_s(tile);
+        const uint32_t t_o = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + C::t_o(tile);
+        const float sl2 = a.scale_log2;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+          if (!mbar_wait_warp(&s_full[tile], j & 1, w, 25)) { ok = false; break; }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, resc)) {
+          const int lim = (j == nkv - 1) ? qi - j * BKV : BKV;  // keys at column > lim are in the future
+          // pass 1: row maximum
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < BKV / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(t_s + c * 32, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
+          }
+          const float m_new = fmaxf(m_run, mx * sl2);
+          float alpha = 1.f;
+          bool resc = false;
+          if (m_new > m_run + kRescaleLog2) {
+            alpha = ex2(m_run - m_new);
+            m_run = m_new;
+            resc = true;
+          }
+          // O (complete up to block j-1, see above) follows a raised reference
+          if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
               uint32_t v[32];
-              const uint32_t ta = tmem + lane_off + 256 + c * 32;
-              tmem_ld32(ta, v);
+              tmem_ld32(t_o + c * 32, v);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              tmem_st32(ta, v);
+              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              tmem_st32(t_o + c * 32, v);
             }
           }
-        }
-        const uint32_t sP = smem_u32(smem + C::P_OFF);
+          // pass 2: P = 2^(s*scale - m) as bf16 pairs into S's first 64 columns;
+          // 64 scores are read before the 32 columns holding their P are written
+          float rs = 0.f;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[32];
 #pragma unroll
-          for (int piece = 0; piece < 8; ++piece) {
-            const uint32_t addr = sP + c * CH + row * 128 + ((piece ^ (row & 7)) << 4);
-            const int b = c * 32 + piece * 4;
-            st_shared_v4(addr, pk[b], pk[b + 1], pk[b + 2], pk[b + 3]);
+            for (int c = 0; c < 2; ++c) {
+              uint32_t v[32];
+              tmem_ld32(t_s + h * 64 + c * 32, v);
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                const int col = h * 64 + c * 32 + e;
+                const float p0 = col <= lim ? ex2(fmaf(__uint_as_float(v[e]), sl2, -m_run)) : 0.f;
+                const float p1 = col + 1 <= lim ? ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -m_run)) : 0.f;
+                rs += p0 + p1;
+                pk[c * 16 + (e >> 1)] = pack_bf16(p0, p1);
+              }
+            }
+            tmem_st32(t_s + h * 32, pk);
           }
+          l_run = l_run * alpha + rs;
+          tc_fence_before();
+          mbar_arrive(&p_ready[tile]);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(p_full);
-      }
-      if (ok && mbar_wait_warp(pv_done, (n_kv - 1) & 1, w, 27)) {
-        tc_fence_after();
-        const float inv = 1.f / l_run;
-        uint16_t* orow = a.O + (static_cast<long long>(slot) * a.S + qi) * D;
+        if (ok && mbar_wait_warp(&o_done[tile], 0, w, 27)) {
+          tc_fence_after();
+          const float inv = 1.f / l_run;
+          uint16_t* orow = a.O + (static_cast<long long>(slot) * a.S + qi) * D;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + 256 + c * 32, v);
-          uint4* o = reinterpret_cast<uint4*>(orow + c * 32);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(t_o + c * 32, v);
+            uint4* o = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            o[i] = make_uint4(pack_bf16(__uint_as_float(v[8 * i]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
-                              pack_bf16(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv),
-                              pack_bf16(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv),
-                              pack_bf16(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
+            for (int i = 0; i < 4; ++i) {
+              o[i] = make_uint4(pack_bf16(__uint_as_float(v[8 * i]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
+                                pack_bf16(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv),
+                                pack_bf16(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv),
+                                pack_bf16(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
+            }
           }
+          a.lse[static_cast<long long>(a.lse_row[slot]) * a.S + qi] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
         }
-        a.lse[static_cast<long long>(a.lse_row[slot]) * a.S + qi] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
       }
     }
   }
@@ -275,7 +300,7 @@ cudaError_t run_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensor
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<args.n_qslots * args.q_blocks, 256, FwdCfg<D>::SMEM, st>>>(tq, tk, tv, args);
+  kern<<<args.n_qslots * args.q_pairs, 384, FwdCfg<D>::SMEM, st>>>(tq, tk, tv, args);
   return cudaGetLastError();
 }
 
@@ -291,6 +316,7 @@ cudaError_t launch_attn_fwd(const AttnFwdDesc& d, int* status, cudaStream_t st) 
   a.S = d.S;
   a.n_qslots = d.n_qslots;
   a.q_blocks = d.S / BQ;
+  a.q_pairs = (a.q_blocks + 1) / 2;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.D)));
   for (int i = 0; i < d.n_qslots; ++i) {
     a.kv_slot[i] = d.kv_slot[i];

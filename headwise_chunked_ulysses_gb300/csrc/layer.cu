@@ -336,6 +336,11 @@ struct Launcher {
     run(UPIPE_KERNEL_HEAD2SEQ, 0.0, b, [&] { return launch_head2seq(p, st); });
     permute_bytes += static_cast<size_t>(b);
   }
+  void dq2s(const DqTiledDesc& p) {
+    const double b = static_cast<double>(p.n_slots) * p.S * p.D * (4 + 2);
+    run(UPIPE_KERNEL_HEAD2SEQ, 0.0, b, [&] { return launch_dq_tiled_to_seq(p, st); });
+    permute_bytes += static_cast<size_t>(b);
+  }
   void prep(const BwdPrepDesc& p) {
     const double b = static_cast<double>(p.n_slots) * p.S * (2.0 * 2 * p.D + 4.0 * p.D + 12.0);
     run(UPIPE_KERNEL_BWD_PREP, 0.0, b, [&] { return launch_bwd_prep(p, st); });
@@ -581,36 +586,36 @@ int upipe_attn_bwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
     ab.dK = dacc + U * slot_elems;
     ab.dV = dacc + (U + p.n_kv_slots) * slot_elems;
     ab.accumulate_kv = (ooo && i > 0) ? 1 : 0;
+    ab.dq_tiled = 1;
     ab.S = S; ab.D = d; ab.n_qslots = U; ab.n_kvslots = p.n_kv_slots;
     for (int k = 0; k < U; ++k) ab.kv_slot[k] = static_cast<uint16_t>(g.kv_of_q[k]);
     L.bwd(ab);
     // exchange back: dQ (and in order, the summed copies of dK and dV) into the sequence buffer
-    Head2SeqDesc hb;
-    hb.src = dacc; hb.src_f32 = true;
-    hb.dst = seq; hb.S = S; hb.D = d;
-    std::vector<int> wheads;
-    int n = 0, r = 0;
-    hb.first[0] = 0;
-    for (int k = 0; k < U; ++k) {
-      hb.dst_head[n] = static_cast<uint16_t>(n);
-      hb.src_slot[r++] = static_cast<uint16_t>(k);
-      hb.first[++n] = static_cast<uint16_t>(r);
-      wheads.push_back(g.q_heads[k]);
-    }
-    if (!ooo) {
-      const int nkv = static_cast<int>(g.kv_proj.size());
+    std::vector<int> wheads(g.q_heads.begin(), g.q_heads.end());
+    const int nkv = ooo ? 0 : static_cast<int>(g.kv_proj.size());
+    for (int part = 0; part < 2; ++part)
+      for (int m = 0; m < nkv; ++m) wheads.push_back((part == 0 ? H : H + G) + g.kv_proj[m]);
+    const long long ld_dseq = static_cast<long long>(wheads.size()) * d;
+    DqTiledDesc qb;
+    qb.src = dacc; qb.dst = seq; qb.ld_dst = ld_dseq; qb.S = S; qb.D = d; qb.n_slots = U;
+    for (int k = 0; k < U; ++k) qb.dst_head[k] = static_cast<uint16_t>(k);
+    L.dq2s(qb);
+    if (nkv > 0) {
+      Head2SeqDesc hb;
+      hb.src = dacc; hb.src_f32 = true;
+      hb.dst = seq; hb.ld_dst = ld_dseq; hb.S = S; hb.D = d;
+      int n = 0, r = 0;
+      hb.first[0] = 0;
       for (int part = 0; part < 2; ++part)
         for (int m = 0; m < nkv; ++m) {
-          hb.dst_head[n] = static_cast<uint16_t>(n);
+          hb.dst_head[n] = static_cast<uint16_t>(U + n);
           for (int k = 0; k < p.n_kv_slots; ++k)
             if (g.k_src[k] == m) hb.src_slot[r++] = static_cast<uint16_t>(U + part * p.n_kv_slots + k);
           hb.first[++n] = static_cast<uint16_t>(r);
-          wheads.push_back((part == 0 ? H : H + G) + g.kv_proj[m]);
         }
+      hb.n_heads = n;
+      L.h2s(hb);
     }
-    hb.n_heads = n;
-    hb.ld_dst = static_cast<long long>(n) * d;
-    L.h2s(hb);
     project_back(seq, wheads);
   }
   if (ooo && L.ok()) {

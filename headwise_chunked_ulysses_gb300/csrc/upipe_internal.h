@@ -57,7 +57,11 @@ struct AttnBwdDesc {
   const void* dO = nullptr;  // [n_qslots][S][D] bf16
   const float* lse2 = nullptr;  // [n_qslots][S]  log2-domain log-sum-exp
   const float* Dsum = nullptr;  // [n_qslots][S]  rowsum(dO * O)
-  float* dQacc = nullptr;    // [n_qslots][S][D] fp32, pre-zeroed, atomically accumulated (unscaled)
+  float* dQacc = nullptr;    // fp32 per query slot, pre-zeroed, atomically accumulated
+  // dQacc layout: 0 = [slot][S][D] row-major; 1 = tiled [slot][S/32][D/4][32][4]
+  // (32 consecutive rows of one 4-wide column group contiguous, so one warp's
+  // vector reduction covers a single 512-byte run)
+  int dq_tiled = 0;
   float* dK = nullptr;       // [n_kvslots][S][D] fp32
   float* dV = nullptr;       // [n_kvslots][S][D] fp32
   int accumulate_kv = 0;     // add into dK/dV instead of overwriting
@@ -81,6 +85,13 @@ struct Head2SeqDesc {
   uint16_t first[kMaxSlots + 1];    // CSR over source slots per output head
   uint16_t src_slot[kMaxSlots];     // summed in this order (fp32)
 };
+// Tiled fp32 dQ (see AttnBwdDesc::dq_tiled) -> bf16 sequence layout.
+struct DqTiledDesc {
+  const float* src = nullptr;                   // [n_slots][S/32][D/4][32][4]
+  uint16_t* dst = nullptr; long long ld_dst = 0; // bf16 [S][row]
+  int S = 0, D = 0, n_slots = 0;
+  uint16_t dst_head[kMaxSlots];                 // slot -> head block in a dest row
+};
 struct BwdPrepDesc {
   const uint16_t* dO = nullptr; long long ld_do = 0;  // seq layout
   const uint16_t* O = nullptr; long long ld_o = 0;    // seq layout (saved forward output)
@@ -103,6 +114,7 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& a, int* status, cudaStream_t st);
 cudaError_t launch_seq2head(const Seq2HeadDesc& p, cudaStream_t st);
 cudaError_t launch_head2seq(const Head2SeqDesc& p, cudaStream_t st);
 cudaError_t launch_bwd_prep(const BwdPrepDesc& p, cudaStream_t st);
+cudaError_t launch_dq_tiled_to_seq(const DqTiledDesc& p, cudaStream_t st);
 
 // Tensor maps (driver entry point resolved through the runtime).
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
