@@ -269,7 +269,8 @@ def attention_bwd_noalloc(Q, K, V, O, dO, lse, kv_of_q, dQ, dK, dV, stream=None)
 
 
 def gemm(A, B, M, N, K, a_trans, b_trans, out_mode=1, D=None, stream=None):
-    """D = A B on the tensor cores (see upipe_gemm_bf16).  out_mode 0 bf16, 1 fp32, 2 fp32 +=."""
+    """D = A B on the tensor cores (see upipe_gemm_bf16).  out_mode 0 bf16, 1 fp32, 2 fp32 +=,
+    3 fp32 += with split-K partial sums added atomically."""
     torch = _torch()
     bf = torch.bfloat16
     if D is None:

@@ -26,16 +26,17 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+def sources(src_dir: str = CSRC):
+    return sorted(os.path.join(src_dir, f) for f in os.listdir(src_dir) if f.endswith(".cu"))
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
+def build(verbose: bool = False, extra_flags=(), src_dir: str = CSRC, lib_path: str = LIB) -> str:
+    """Compile every .cu file of src_dir and link them into lib_path."""
     nvcc = _nvcc()
-    obj_dir = os.path.join(OUT_DIR, "obj")
+    obj_dir = os.path.join(os.path.dirname(lib_path), "obj_" + os.path.basename(lib_path).replace(".", "_"))
     os.makedirs(obj_dir, exist_ok=True)
     flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
-                    "-I" + os.path.join(ROOT, "include"), "-I" + CSRC] + list(extra_flags)
+                    "-I" + os.path.join(ROOT, "include"), "-I" + src_dir] + list(extra_flags)
 
     def compile_one(src):
         obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
@@ -47,16 +48,16 @@ def build(verbose: bool = False, extra_flags=()) -> str:
             print(" ".join(cmd))
         return obj
 
-    srcs = sources()
+    srcs = sources(src_dir)
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -209,12 +209,12 @@ __global__ void __launch_bounds__(384, 1)
           // pass 1: row maximum
           float mx = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < BKV / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(t_s + c * 32, v);
+          for (int c = 0; c < BKV / 64; ++c) {
+            uint32_t v[64];
+            tmem_ld64(t_s + c * 64, v);
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (c * 32 + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
+            for (int e = 0; e < 64; ++e)
+              if (c * 64 + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
           }
           const float m_new = fmaxf(m_run, mx * sl2);
           float alpha = 1.f;

@@ -27,7 +27,7 @@ constexpr int BOX_BYTES = 64 * 64 * 2;  // one 64x64 bf16 box: 64 rows of 128 B
 
 struct GemmArgs {
   int M, N, K;
-  int m_tiles, n_tiles;
+  int m_tiles, n_tiles, split_k;
   int use_amap_k, use_bmap_k, use_bmap_n, use_omap_n;
   uint16_t amap_k[kMaxMap];
   uint16_t bmap_k[kMaxMap];
@@ -53,7 +53,13 @@ struct Cfg {
 };
 
 __device__ __forceinline__ void store_tile_chunk(const GemmArgs& g, int m, int oc, const uint32_t (&v)[32]) {
-  if (g.out_mode == kOutF32 || g.out_mode == kOutF32Acc) {
+  if (g.out_mode == kOutF32Red) {  // split-K partial sums: vector reductions
+    float* o = static_cast<float*>(g.out) + (long long)m * g.ldo + oc;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      red_add_v4(o + 4 * i, __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                 __uint_as_float(v[4 * i + 3]));
+  } else if (g.out_mode == kOutF32 || g.out_mode == kOutF32Acc) {
     float4* o = reinterpret_cast<float4*>(static_cast<float*>(g.out) + (long long)m * g.ldo + oc);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -129,8 +135,12 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n_tiles = g.m_tiles * g.n_tiles;
-  const int kblocks = g.K / BK;
+  const int n_tiles = g.m_tiles * g.n_tiles * g.split_k;
+  const int kblocks = g.K / BK / g.split_k;  // k blocks per tile
+  // tile t: split ks = t / (m_tiles*n_tiles), then m-major, n fastest
+  auto tile_m0 = [&](int t) { return ((t % (g.m_tiles * g.n_tiles)) / g.n_tiles) * BM; };
+  auto tile_n0 = [&](int t) { return (t % g.n_tiles) * BN; };
+  auto tile_kb0 = [&](int t) { return (t / (g.m_tiles * g.n_tiles)) * kblocks; };
 
   if (aligned) {
     if (warp == 0 && lane == 0) {
@@ -138,8 +148,8 @@ __global__ void __launch_bounds__(256, 1)
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
-        const int m0 = (t / g.n_tiles) * BM, n0 = (t % g.n_tiles) * BN;
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        const int m0 = tile_m0(t), n0 = tile_n0(t), kb0 = tile_kb0(t);
+        for (int kb = kb0; kb < kb0 + kblocks; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, w, 1)) { ok = false; break; }
@@ -197,8 +207,8 @@ __global__ void __launch_bounds__(256, 1)
         const int acc = tl & 1;
         if (!mbar_wait_warp(&tfull[acc], (tl >> 1) & 1, w, 4)) break;
         tc_fence_after();
-        const int m = (t / g.n_tiles) * BM + row;
-        const int n0 = (t % g.n_tiles) * BN;
+        const int m = tile_m0(t) + row;
+        const int n0 = tile_n0(t);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
@@ -229,7 +239,7 @@ cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& ar
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int tiles = args.m_tiles * args.n_tiles;
+  const int tiles = args.m_tiles * args.n_tiles * args.split_k;
   const int grid = std::min(tiles, num_sms());
   kern<<<grid, 256, Cfg<BN>::SMEM, st>>>(ta, tb, args);
   return cudaGetLastError();
@@ -253,6 +263,8 @@ void copy_map(const BlockMap& m, int& use, uint16_t* dst) {
 
 cudaError_t launch_gemm(const GemmDesc& d, int* status, cudaStream_t st) {
   if (d.M % BM || d.K % BK || d.N % 64 || d.M <= 0 || d.N <= 0 || d.K <= 0) return cudaErrorInvalidValue;
+  if (d.split_k < 1 || (d.K / BK) % d.split_k || (d.split_k > 1 && d.out_mode != kOutF32Red))
+    return cudaErrorInvalidValue;
   const int BN = (d.N % 256 == 0) ? 256 : (d.N % 128 == 0 ? 128 : 64);
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, d.A, d.a_cols, d.a_rows, d.lda, 64, 64)) return cudaErrorInvalidValue;
@@ -261,6 +273,7 @@ cudaError_t launch_gemm(const GemmDesc& d, int* status, cudaStream_t st) {
   a.M = d.M; a.N = d.N; a.K = d.K;
   a.m_tiles = d.M / BM;
   a.n_tiles = d.N / BN;
+  a.split_k = d.split_k;
   copy_map(d.amap_k, a.use_amap_k, a.amap_k);
   copy_map(d.bmap_k, a.use_bmap_k, a.bmap_k);
   copy_map(d.bmap_n, a.use_bmap_n, a.bmap_n);

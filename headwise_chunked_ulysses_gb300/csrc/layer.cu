@@ -239,6 +239,21 @@ Plan make_plan(const Shape& s, bool backward) {
   return p;
 }
 
+// Split of a long-K contraction so that its output tiles fill the GPU: the
+// smallest split giving at least 4 tiles per SM, K/64 divisible by it.
+int choose_split_k(const GemmDesc& g) {
+  const int bn = (g.N % 256 == 0) ? 256 : (g.N % 128 == 0 ? 128 : 64);
+  const long long tiles = static_cast<long long>(g.M / 128) * (g.N / bn);
+  const int kb = g.K / 64;
+  int best = 1;
+  for (int s = 1; s <= 16; ++s) {
+    if (kb % s || kb / s < 8) continue;
+    best = s;
+    if (tiles * s >= 4LL * num_sms()) break;
+  }
+  return best;
+}
+
 // 64-element blocks of the given heads (d columns each), in order
 void head_blocks(BlockMap& m, const std::vector<int>& cols_in_heads, int d) {
   m.n = 0;
@@ -543,7 +558,8 @@ int upipe_attn_bwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
     gw.B = dseq; gw.ldb = static_cast<long long>(ncols) * d; gw.b_rows = S; gw.b_cols = gw.ldb; gw.b_mn = true;
     gw.M = d_model; gw.N = ncols * d; gw.K = S;
     head_blocks(gw.omap_n, wheads, d);
-    gw.out = dW_qkv; gw.ldo = qkv_ld; gw.out_mode = kOutF32Acc;
+    gw.out = dW_qkv; gw.ldo = qkv_ld; gw.out_mode = kOutF32Red;  // dW_qkv is zeroed above
+    gw.split_k = choose_split_k(gw);
     L.gemm(gw);
   };
 
@@ -644,7 +660,14 @@ int upipe_attn_bwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
   gwo.A = O_saved; gwo.lda = static_cast<long long>(H) * d; gwo.a_rows = S; gwo.a_cols = gwo.lda; gwo.a_mn = true;
   gwo.B = dY; gwo.ldb = d_model; gwo.b_rows = S; gwo.b_cols = d_model; gwo.b_mn = true;
   gwo.M = H * d; gwo.N = d_model; gwo.K = S;
-  gwo.out = dW_o; gwo.ldo = d_model; gwo.out_mode = kOutF32;
+  gwo.out = dW_o; gwo.ldo = d_model;
+  gwo.split_k = choose_split_k(gwo);
+  if (gwo.split_k > 1) {
+    if (cudaMemsetAsync(dW_o, 0, static_cast<size_t>(H) * d * d_model * 4, L.st) != cudaSuccess) return UPIPE_ECUDA;
+    gwo.out_mode = kOutF32Red;
+  } else {
+    gwo.out_mode = kOutF32;
+  }
   L.gemm(gwo);
   return finish(L, p, stats);
 }
@@ -755,7 +778,7 @@ int upipe_gemm_bf16(const upipe_bf16* A, const upipe_bf16* B, void* D, int M, in
                     long long lda, long long ldb, long long ldd, int out_mode, void* stream) {
   if (!A || !B || !D || !aligned16(A) || !aligned16(B) || !aligned16(D)) return UPIPE_EINVAL;
   if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 64 || K % 64) return UPIPE_EINVAL;
-  if (out_mode < 0 || out_mode > 2 || lda % 8 || ldb % 8 || ldd % 8) return UPIPE_EINVAL;
+  if (out_mode < 0 || out_mode > 3 || lda % 8 || ldb % 8 || ldd % 8) return UPIPE_EINVAL;
   if (!device_supported()) return UPIPE_EUNSUPPORTED;
   int* status = status_ptr();
   if (!status) return UPIPE_ECUDA;
@@ -767,7 +790,8 @@ int upipe_gemm_bf16(const upipe_bf16* A, const upipe_bf16* B, void* D, int M, in
   if (g.a_cols > lda || g.b_cols > ldb) return UPIPE_EINVAL;
   g.M = M; g.N = N; g.K = K;
   g.out = D; g.ldo = ldd;
-  g.out_mode = out_mode == 0 ? kOutBf16 : (out_mode == 1 ? kOutF32 : kOutF32Acc);
+  g.out_mode = out_mode == 0 ? kOutBf16 : (out_mode == 1 ? kOutF32 : (out_mode == 2 ? kOutF32Acc : kOutF32Red));
+  if (out_mode == 3) g.split_k = choose_split_k(g);
   return launch_gemm(g, status, static_cast<cudaStream_t>(stream)) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
 }
 

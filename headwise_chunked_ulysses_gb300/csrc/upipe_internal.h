@@ -23,6 +23,7 @@ enum GemmOut : int {
   kOutF32 = 1,         // out(fp32)  = acc
   kOutF32Acc = 2,      // out(fp32) += acc
   kOutBf16PlusF32 = 3, // out(bf16)  = acc + aux(fp32)
+  kOutF32Red = 4,      // out(fp32) += acc with vector atomics (split-K partial sums)
 };
 
 // D[M,N] = A[M,K] * B[K,N], bf16 operands, fp32 accumulation.
@@ -37,6 +38,7 @@ struct GemmDesc {
   BlockMap amap_k, bmap_k, bmap_n, omap_n;
   void* out = nullptr; long long ldo = 0; int out_mode = kOutF32;
   const float* aux = nullptr; long long ld_aux = 0;
+  int split_k = 1;  // > 1 only with kOutF32Red: K is cut into split_k equal ranges
 };
 
 struct AttnFwdDesc {

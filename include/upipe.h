@@ -200,7 +200,9 @@ int upipe_attention_bwd_noalloc(const upipe_bf16* Q, const upipe_bf16* K, const 
  * output projection): D[M,N] = A[M,K] B[K,N], bf16 in, fp32 accumulate.
  *   A : device bf16, stored [M][K] (a_trans == 0) or [K][M] (a_trans == 1), row stride lda.
  *   B : device bf16, stored [K][N] (b_trans == 0) or [N][K] (b_trans == 1), row stride ldb.
- *   out_mode 0: D bf16;  1: D fp32;  2: D fp32 += A B.  ldd: row stride of D.
+ *   out_mode 0: D bf16;  1: D fp32;  2: D fp32 += A B;  3: D fp32 += A B with K
+ *   split across CTAs and the partial sums added by fp32 atomics (for few output
+ *   tiles and a long K; the summation order varies between runs).  ldd: row stride of D.
  * M % 128 == 0, N % 64 == 0, K % 64 == 0.
  */
 int upipe_gemm_bf16(const upipe_bf16* A, const upipe_bf16* B, void* D, int M, int N, int K, int a_trans, int b_trans,

@@ -2,8 +2,9 @@
 
 * the Ulysses exchange (seq->head, head->seq): bit-exact against the oracle's
   all-to-all of C virtual ranks;
-* the tensor-core contraction in all four operand layouts and three output
-  modes: against an fp64 product of the same bf16 operands;
+* the tensor-core contraction in all four operand layouts and four output
+  modes (incl. split-K with atomic partial sums): against an fp64 product of
+  the same bf16 operands;
 * causal GQA attention forward and backward: against the oracle's attention
   core (fp64), per head; dK, dV summed over the query heads of each group.
 """
@@ -61,7 +62,8 @@ def test_exchange_is_bit_exact(up, S, n_heads, d, C, pad):
 # contraction
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("M,N,K", [(256, 384, 320), (128, 512, 128), (384, 64, 192), (256, 256, 1024)])
+@pytest.mark.parametrize("M,N,K", [(256, 384, 320), (128, 512, 128), (384, 64, 192), (256, 256, 1024),
+                                   (128, 256, 8192)])
 @pytest.mark.parametrize("a_trans,b_trans", [(0, 0), (0, 1), (1, 0), (1, 1)])
 def test_gemm_layouts_and_modes(up, M, N, K, a_trans, b_trans):
     import torch
@@ -78,6 +80,10 @@ def test_gemm_layouts_and_modes(up, M, N, K, a_trans, b_trans):
     base = torch.randn(M, N, dtype=torch.float32, device="cuda")
     base0 = f64_of(base)
     up.gemm(A, B, M, N, K, a_trans, b_trans, out_mode=2, D=base)
+    assert rel(f64_of(base), base0 + want) < 1e-5
+    base = torch.randn(M, N, dtype=torch.float32, device="cuda")
+    base0 = f64_of(base)
+    up.gemm(A, B, M, N, K, a_trans, b_trans, out_mode=3, D=base)  # split-K, atomic partial sums
     assert rel(f64_of(base), base0 + want) < 1e-5
     up.sync_status()
 
