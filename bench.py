@@ -101,6 +101,24 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
+def max_over_ranks(value, device=None):
+    """The largest of a per-rank float over the default process group (the
+    value itself when no group is initialised)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tokens_per_s(world, tokens_per_rank_step, steps, max_elapsed_ms):
+    """Whole-job throughput: every rank processes its own replica of the
+    workload; the job takes as long as the slowest rank."""
+    return world * tokens_per_rank_step * steps / (max_elapsed_ms / 1e3)
+
+
 def model_flops_step(sh):
     """Model FLOPs of one fwd+bwd step: 3x the forward, which is the QKV
     projection, the output projection and causal attention (QK^T and PV over
@@ -357,13 +375,9 @@ def main():
     upipe.profile_enable(False)
     clk = clocks.stop()
     upipe.sync_status()
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     ms_step = elapsed_ms / args.steps
-    tokens_per_s = world * sh.S * args.steps / (elapsed_ms / 1e3)
+    tokens_per_s = aggregate_tokens_per_s(world, sh.S, args.steps, elapsed_ms)
     pk = peaks()
     flops_step = model_flops_step(sh)
     tflops = flops_step / (ms_step / 1e3) / 1e12
@@ -424,13 +438,8 @@ def main():
             e2e_step()
         f1.record(stream)
         barrier()
-        e_ms = f0.elapsed_time(f1)
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * sh.S * args.steps / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e_ms = max_over_ranks(f0.elapsed_time(f1), dev)
+        e2e = {"value": aggregate_tokens_per_s(world, sh.S, args.steps, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps}
         upipe.sync_status()
 
