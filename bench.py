@@ -101,6 +101,36 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
+KERNEL_SOURCES = {"attn_bwd": "attn_bwd.cu", "attn_fwd": "attn_fwd.cu", "gemm": "gemm.cu",
+                  "seq2head": "permute.cu", "head2seq": "permute.cu", "bwd_prep": "attn_bwd.cu"}
+
+
+def source_sha(kernel):
+    import hashlib
+    path = os.path.join(ROOT, "headwise_chunked_ulysses_gb300", "csrc", KERNEL_SOURCES[kernel])
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    profiles/traffic_<kernel>_<workload>.md, if that capture was taken from
+    the current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_sha256_16") != source_sha(kernel):
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def max_over_ranks(value, device=None):
     """The largest of a per-rank float over the default process group (the
     value itself when no group is initialised)."""
@@ -403,13 +433,15 @@ def main():
         achieved = fl_launch / (ms_dom / n_dom / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": achieved / peak_tf, "peak_source": f"{pk['source']} bf16_tflops_sustained",
-                "flops_per_launch": fl_launch, "ms_per_launch": ms_dom / n_dom, "traffic": None}
+                "flops_per_launch": fl_launch, "ms_per_launch": ms_dom / n_dom,
+                "traffic": measured_traffic(dom, args.workload), "source_sha256_16": source_sha(dom)}
     else:
         by_launch = (stf["bytes_by_kind"][dom] + stb["bytes_by_kind"][dom]) / max(1, kernels[dom]["launches_per_step"])
         achieved = by_launch / (ms_dom / n_dom / 1e3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"], "peak_source": f"{pk['source']} hbm_gbs",
-                "bytes_per_launch": by_launch, "ms_per_launch": ms_dom / n_dom, "traffic": None}
+                "bytes_per_launch": by_launch, "ms_per_launch": ms_dom / n_dom,
+                "traffic": measured_traffic(dom, args.workload), "source_sha256_16": source_sha(dom)}
     launches = (stf["launches"] + stb["launches"]) * args.steps
 
     # ---------------- end to end through the public API, host buffers ----------------

@@ -205,16 +205,22 @@ __global__ void __launch_bounds__(384, 1)
         for (int j = 0; j < nkv; ++j) {
           if (!mbar_wait_warp(&s_full[tile], j & 1, w, 25)) { ok = false; break; }
           tc_fence_after();
-          const int lim = (j == nkv - 1) ? qi - j * BKV : BKV;  // keys at column > lim are in the future
+          const bool diag = (j == nkv - 1);
+          const int lim = diag ? qi - j * BKV : BKV;  // keys at column > lim are in the future
           // pass 1: row maximum
           float mx = -INFINITY;
 #pragma unroll
           for (int c = 0; c < BKV / 64; ++c) {
             uint32_t v[64];
             tmem_ld64(t_s + c * 64, v);
+            if (diag) {
 #pragma unroll
-            for (int e = 0; e < 64; ++e)
-              if (c * 64 + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
+              for (int e = 0; e < 64; ++e)
+                if (c * 64 + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
+            } else {
+#pragma unroll
+              for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+            }
           }
           const float m_new = fmaxf(m_run, mx * sl2);
           float alpha = 1.f;
@@ -245,13 +251,23 @@ __global__ void __launch_bounds__(384, 1)
             for (int c = 0; c < 2; ++c) {
               uint32_t v[32];
               tmem_ld32(t_s + h * 64 + c * 32, v);
+              if (diag) {
 #pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                const int col = h * 64 + c * 32 + e;
-                const float p0 = col <= lim ? ex2(fmaf(__uint_as_float(v[e]), sl2, -m_run)) : 0.f;
-                const float p1 = col + 1 <= lim ? ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -m_run)) : 0.f;
-                rs += p0 + p1;
-                pk[c * 16 + (e >> 1)] = pack_bf16(p0, p1);
+                for (int e = 0; e < 32; e += 2) {
+                  const int col = h * 64 + c * 32 + e;
+                  const float p0 = col <= lim ? ex2(fmaf(__uint_as_float(v[e]), sl2, -m_run)) : 0.f;
+                  const float p1 = col + 1 <= lim ? ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -m_run)) : 0.f;
+                  rs += p0 + p1;
+                  pk[c * 16 + (e >> 1)] = pack_bf16(p0, p1);
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                  const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, -m_run));
+                  const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -m_run));
+                  rs += p0 + p1;
+                  pk[c * 16 + (e >> 1)] = pack_bf16(p0, p1);
+                }
               }
             }
             tmem_st32(t_s + h * 32, pk);
