@@ -178,11 +178,13 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t sDS = smem_u32(smem + C::DS_TILE_OFF);
       auto sQ = [&](int st) { return smem_u32(smem + C::Q_OFF + st * C::TILE); };
       auto sdO = [&](int st) { return smem_u32(smem + C::DO_OFF + st * C::TILE); };
+      // operand descriptors are built once per tile and advanced by constants
       auto qk_mma = [&](uint32_t d_tmem, uint32_t sA, uint32_t sB) {
+        const uint64_t a0 = sdesc_kmajor(sA), b0 = sdesc_kmajor(sB);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * CH + (k & 3) * 32;
-          mma_ss(d_tmem, sdesc_kmajor(sA + off), sdesc_kmajor(sB + off), ID_S, k > 0);
+          mma_ss(d_tmem, sdesc_advance(a0, off), sdesc_advance(b0, off), ID_S, k > 0);
         }
       };
       bool ok = mbar_wait(kv_full, 0, w, 41) && mbar_wait(&qdo_full[0], 0, w, 42);
@@ -199,10 +201,13 @@ __global__ void __launch_bounds__(384, 1)
         // columns [0,64) at S^T columns [0,32), [64,128) at [64,96)
         if (!mbar_wait(p_ready, i & 1, w, 43)) break;
         tc_fence_after();
+        {
+          const uint64_t b0 = sdesc_mnmajor(sdO(st), CH);
 #pragma unroll
-        for (int k = 0; k < BQ / 16; ++k)
-          mma_ts(tmem + C::T_DV, tmem + C::T_S + (k >> 2) * 64 + (k & 3) * 8, sdesc_mnmajor(sdO(st) + k * 2048, CH),
-                 ID_KV, (i | k) != 0);
+          for (int k = 0; k < BQ / 16; ++k)
+            mma_ts(tmem + C::T_DV, tmem + C::T_S + (k >> 2) * 64 + (k & 3) * 8, sdesc_advance(b0, k * 2048), ID_KV,
+                   (i | k) != 0);
+        }
         // next S^T: issued after dV_i, so it overwrites P^T_i only once dV_i has read it
         if (i + 1 < n_items) {
           if (!mbar_wait(&qdo_full[st ^ 1], ((i + 1) >> 1) & 1, w, 44)) break;
@@ -213,15 +218,17 @@ __global__ void __launch_bounds__(384, 1)
         // dK += dS^T Q ; dQ = dS K (into dP's columns, read already)
         if (!mbar_wait(ds_ready, i & 1, w, 45)) break;
         tc_fence_after();
+        {
+          const uint64_t a0 = sdesc_kmajor(sDS), b0 = sdesc_mnmajor(sQ(st), CH);
 #pragma unroll
-        for (int k = 0; k < BQ / 16; ++k) {
-          const uint32_t poff = (k >> 2) * CH + (k & 3) * 32;
-          mma_ss(tmem + C::T_DK, sdesc_kmajor(sDS + poff), sdesc_mnmajor(sQ(st) + k * 2048, CH), ID_KV,
-                 (i | k) != 0);
+          for (int k = 0; k < BQ / 16; ++k)
+            mma_ss(tmem + C::T_DK, sdesc_advance(a0, (k >> 2) * CH + (k & 3) * 32), sdesc_advance(b0, k * 2048), ID_KV,
+                   (i | k) != 0);
+          const uint64_t a1 = sdesc_mnmajor(sDS, CH), b1 = sdesc_mnmajor(sK, CH);
+#pragma unroll
+          for (int k = 0; k < BKV / 16; ++k)
+            mma_ss(tmem + C::T_DP, sdesc_advance(a1, k * 2048), sdesc_advance(b1, k * 2048), ID_Q, k > 0);
         }
-#pragma unroll
-        for (int k = 0; k < BKV / 16; ++k)
-          mma_ss(tmem + C::T_DP, sdesc_mnmajor(sDS + k * 2048, CH), sdesc_mnmajor(sK + k * 2048, CH), ID_Q, k > 0);
         mma_commit(ds_consumed);
         mma_commit(dq_full);
         mma_commit(&qdo_empty[st]);

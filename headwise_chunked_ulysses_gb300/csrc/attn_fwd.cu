@@ -146,11 +146,11 @@ __global__ void __launch_bounds__(384, 1)
         const int s = j & 1;
         if (!mbar_wait(&k_full[s], (j >> 1) & 1, w, 22)) return false;
         tc_fence_after();
-        const uint32_t sK = smem_u32(smem + C::K_OFF + s * C::TILE);
+        const uint64_t a0 = sdesc_kmajor(sQ[tile]), b0 = sdesc_kmajor(smem_u32(smem + C::K_OFF + s * C::TILE));
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * CH + (k & 3) * 32;
-          mma_ss(tmem + C::t_s(tile), sdesc_kmajor(sQ[tile] + off), sdesc_kmajor(sK + off), ID_S, k > 0);
+          mma_ss(tmem + C::t_s(tile), sdesc_advance(a0, off), sdesc_advance(b0, off), ID_S, k > 0);
         }
         mma_commit(&s_full[tile]);
         return true;
@@ -160,11 +160,10 @@ __global__ void __launch_bounds__(384, 1)
         if (!mbar_wait(&p_ready[tile], j & 1, w, 23)) return false;
         if (!mbar_wait(&v_full[s], (j >> 1) & 1, w, 24)) return false;
         tc_fence_after();
-        const uint32_t sV = smem_u32(smem + C::V_OFF + s * C::TILE);
+        const uint64_t b0 = sdesc_mnmajor(smem_u32(smem + C::V_OFF + s * C::TILE), CH);
 #pragma unroll
         for (int k = 0; k < BKV / 16; ++k)
-          mma_ts(tmem + C::t_o(tile), tmem + C::t_s(tile) + k * 8, sdesc_mnmajor(sV + k * 2048, CH), ID_O,
-                 (j | k) != 0);
+          mma_ts(tmem + C::t_o(tile), tmem + C::t_s(tile) + k * 8, sdesc_advance(b0, k * 2048), ID_O, (j | k) != 0);
         return true;
       };
       if (ok) ok = issue_s(0, 0);

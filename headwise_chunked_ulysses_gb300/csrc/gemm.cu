@@ -188,10 +188,12 @@ __global__ void __launch_bounds__(256, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * C::STAGE_BYTES);
           const uint32_t sb = sa + C::A_BYTES;
+          const uint64_t a0 = A_MN ? sdesc_mnmajor(sa, BOX_BYTES) : sdesc_kmajor(sa);
+          const uint64_t b0 = B_MN ? sdesc_mnmajor(sb, BOX_BYTES) : sdesc_kmajor(sb);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = A_MN ? sdesc_mnmajor(sa + k * 2048, BOX_BYTES) : sdesc_kmajor(sa + k * 32);
-            const uint64_t bd = B_MN ? sdesc_mnmajor(sb + k * 2048, BOX_BYTES) : sdesc_kmajor(sb + k * 32);
+            const uint64_t ad = sdesc_advance(a0, A_MN ? k * 2048 : k * 32);
+            const uint64_t bd = sdesc_advance(b0, B_MN ? k * 2048 : k * 32);
             mma_ss(d_tmem, ad, bd, IDESC, (kb | k) != 0);
           }
           mma_commit(&empty[s]);
@@ -228,6 +230,203 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Paired-CTA variant: a cluster of two CTAs computes a 256 x 256 output tile
+// with the M=256 form of the MMA.  CTA r of the pair loads A rows
+// [m0 + 128r, +128) and B columns [n0 + 128r, +128) of each 64-deep K block
+// into its own shared memory, so each SM reads and writes half of B compared
+// with one CTA computing 128 x 256: the shared-memory traffic per MMA falls
+// from about 1.5x to about 1x of what one SM can move.  CTA 0 issues the MMAs
+// (operands at the same shared offsets in both CTAs) and owns the pair's "full"
+// barriers, on which both CTAs' TMA loads complete; MMA completion is
+// multicast to both CTAs' "empty" and "accumulator full" barriers; each CTA
+// drains its own 128 accumulator rows and reports to CTA 0's "accumulator
+// empty" barrier.
+// ---------------------------------------------------------------------------
+struct Cfg2 {
+  static constexpr int STAGES = 6;
+  static constexpr int A_BYTES = 128 * BK * 2;   // this CTA's A rows
+  static constexpr int B_BYTES = 128 * BK * 2;   // this CTA's B columns
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 512;          // two 256-column accumulators
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int SMEM = BAR_OFF + 256;
+};
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(256, 1)
+    gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ GemmArgs g) {
+  using C = Cfg2;
+  constexpr int STAGES = C::STAGES;
+  constexpr int BNP = 256;  // output columns per pair tile
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);  // used in CTA 0
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;  // used in CTA 0
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const Watch w{abort_flag, g.status};
+  const bool aligned = (smem_u32(smem) & 1023u) == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 256);  // both CTAs' epilogue threads
+    }
+    *abort_flag = aligned ? 0 : 1;
+    if (!aligned && g.status) atomicCAS(g.status, 0, kDevBadSmem);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int pair = static_cast<int>(blockIdx.x) >> 1, n_pairs = static_cast<int>(gridDim.x) >> 1;
+  const int n_tiles = g.m_tiles * g.n_tiles * g.split_k;  // m_tiles counts 256-row tiles here
+  const int kblocks = g.K / BK / g.split_k;
+  auto tile_m0 = [&](int t) { return ((t % (g.m_tiles * g.n_tiles)) / g.n_tiles) * 256; };
+  auto tile_n0 = [&](int t) { return (t % g.n_tiles) * BNP; };
+  auto tile_kb0 = [&](int t) { return (t / (g.m_tiles * g.n_tiles)) * kblocks; };
+  const uint32_t full0 = mapa_shared(smem_u32(full), 0);     // CTA 0's full[0]
+  const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0); // CTA 0's tempty[0]
+
+  if (aligned) {
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      int it = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < n_tiles; t += n_pairs) {
+        const int m0 = tile_m0(t) + 128 * static_cast<int>(rank), n0 = tile_n0(t) + 128 * static_cast<int>(rank);
+        const int kb0 = tile_kb0(t);
+        for (int kb = kb0; kb < kb0 + kblocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, w, 61)) { ok = false; break; }
+          uint8_t* sa = smem + s * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::A_BYTES;
+          const uint32_t fb = full0 + s * 8;
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
+          const int ka = (g.use_amap_k ? g.amap_k[kb] : kb) * BK;
+          const int kbb = (g.use_bmap_k ? g.bmap_k[kb] : kb) * BK;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if (A_MN) tma_load_2d_pair(sa + i * BOX_BYTES, &tmA, fb, m0 + 64 * i, ka);
+            else      tma_load_2d_pair(sa + i * BOX_BYTES, &tmA, fb, ka, m0 + 64 * i);
+          }
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int nb = n0 / 64 + i;
+            const int nc = (g.use_bmap_n ? g.bmap_n[nb] : nb) * 64;
+            if (B_MN) tma_load_2d_pair(sb + i * BOX_BYTES, &tmB, fb, nc, kbb);
+            else      tma_load_2d_pair(sb + i * BOX_BYTES, &tmB, fb, kbb, nc);
+          }
+        }
+      }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (CTA 0 only) ----------------
+      constexpr uint32_t IDESC = idesc_bf16(256, BNP, A_MN, B_MN);
+      int it = 0, tl = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < n_tiles; t += n_pairs, ++tl) {
+        const int acc = tl & 1;
+        if (!mbar_wait(&tempty[acc], ((tl >> 1) & 1) ^ 1, w, 62)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * BNP;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&full[s], (it / STAGES) & 1, w, 63)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
+          const uint64_t a0 = A_MN ? sdesc_mnmajor(sa, BOX_BYTES) : sdesc_kmajor(sa);
+          const uint64_t b0 = B_MN ? sdesc_mnmajor(sb, BOX_BYTES) : sdesc_kmajor(sb);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = sdesc_advance(a0, A_MN ? k * 2048 : k * 32);
+            const uint64_t bd = sdesc_advance(b0, B_MN ? k * 2048 : k * 32);
+            mma_ss_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0);
+          }
+          mma_commit_pair(&empty[s]);
+        }
+        if (ok) mma_commit_pair(&tfull[acc]);
+      }
+    } else if (warp >= 4) {
+      // ---------------- epilogue: this CTA's 128 rows of the pair tile ----------------
+      const int q = warp & 3;
+      const int row = q * 32 + lane;
+      int tl = 0;
+      for (int t = pair; t < n_tiles; t += n_pairs, ++tl) {
+        const int acc = tl & 1;
+        if (!mbar_wait_warp(&tfull[acc], (tl >> 1) & 1, w, 64)) break;
+        tc_fence_after();
+        const int m = tile_m0(t) + 128 * static_cast<int>(rank) + row;
+        const int n0 = tile_n0(t);
+#pragma unroll 1
+        for (int c = 0; c < BNP / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BNP + c * 32, v);
+          const int n = n0 + c * 32;
+          const int oc = g.use_omap_n ? g.omap_n[n >> 6] * 64 + (n & 63) : n;
+          store_tile_chunk(g, m, oc, v);
+        }
+        tc_fence_before();
+        mbar_arrive_remote(tempty0 + acc * 8);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while its pair may still touch its shared memory
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::TMEM_COLS);
+  }
+}
+
+template <bool A_MN, bool B_MN>
+cudaError_t run2(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, cudaStream_t st) {
+  auto kern = gemm2_kernel<A_MN, B_MN>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int tiles = args.m_tiles * args.n_tiles * args.split_k;
+  const int pairs = std::min(tiles, num_sms() / 2);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = Cfg2::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
 }
 
 template <int BN, bool A_MN, bool B_MN>
@@ -281,6 +480,13 @@ cudaError_t launch_gemm(const GemmDesc& d, int* status, cudaStream_t st) {
   a.out = d.out; a.ldo = d.ldo; a.out_mode = d.out_mode;
   a.aux = d.aux; a.ld_aux = d.ld_aux;
   a.status = status;
+  if (BN == 256 && d.M % 256 == 0 && num_sms() >= 2) {
+    a.m_tiles = d.M / 256;  // pair tiles of 256 x 256
+    if (d.a_mn && d.b_mn) return run2<true, true>(ta, tb, a, st);
+    if (d.a_mn) return run2<true, false>(ta, tb, a, st);
+    if (d.b_mn) return run2<false, true>(ta, tb, a, st);
+    return run2<false, false>(ta, tb, a, st);
+  }
   if (BN == 256) return dispatch_major<256>(d, ta, tb, a, st);
   if (BN == 128) return dispatch_major<128>(d, ta, tb, a, st);
   return dispatch_major<64>(d, ta, tb, a, st);

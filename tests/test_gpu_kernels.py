@@ -3,8 +3,9 @@
 * the Ulysses exchange (seq->head, head->seq): bit-exact against the oracle's
   all-to-all of C virtual ranks;
 * the tensor-core contraction in all four operand layouts and four output
-  modes (incl. split-K with atomic partial sums): against an fp64 product of
-  the same bf16 operands;
+  modes (incl. split-K with atomic partial sums), on one SM and on CTA pairs
+  (M and N multiples of 256): against an fp64 product of the same bf16
+  operands;
 * causal GQA attention forward and backward: against the oracle's attention
   core (fp64), per head; dK, dV summed over the query heads of each group.
 """
@@ -63,7 +64,7 @@ def test_exchange_is_bit_exact(up, S, n_heads, d, C, pad):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("M,N,K", [(256, 384, 320), (128, 512, 128), (384, 64, 192), (256, 256, 1024),
-                                   (128, 256, 8192)])
+                                   (128, 256, 8192), (512, 512, 512), (768, 1280, 576), (256, 256, 16384)])
 @pytest.mark.parametrize("a_trans,b_trans", [(0, 0), (0, 1), (1, 0), (1, 1)])
 def test_gemm_layouts_and_modes(up, M, N, K, a_trans, b_trans):
     import torch
@@ -73,18 +74,20 @@ def test_gemm_layouts_and_modes(up, M, N, K, a_trans, b_trans):
     A64, B64 = bf16_bits_to_f64(A_bits), bf16_bits_to_f64(B_bits)
     want = (A64.T if a_trans else A64) @ (B64.T if b_trans else B64)
     A, B = to_dev(A_bits), to_dev(B_bits)
+    # fp32 accumulation: rounding error grows like sqrt(K)
+    tol32 = 1e-5 * max(1.0, np.sqrt(K / 1024))
     D32 = up.gemm(A, B, M, N, K, a_trans, b_trans, out_mode=1)
-    assert rel(f64_of(D32), want) < 1e-5
+    assert rel(f64_of(D32), want) < tol32
     D16 = up.gemm(A, B, M, N, K, a_trans, b_trans, out_mode=0)
     assert rel(f64_of(D16), want) < 1e-2
     base = torch.randn(M, N, dtype=torch.float32, device="cuda")
     base0 = f64_of(base)
     up.gemm(A, B, M, N, K, a_trans, b_trans, out_mode=2, D=base)
-    assert rel(f64_of(base), base0 + want) < 1e-5
+    assert rel(f64_of(base), base0 + want) < tol32
     base = torch.randn(M, N, dtype=torch.float32, device="cuda")
     base0 = f64_of(base)
     up.gemm(A, B, M, N, K, a_trans, b_trans, out_mode=3, D=base)  # split-K, atomic partial sums
-    assert rel(f64_of(base), base0 + want) < 1e-5
+    assert rel(f64_of(base), base0 + want) < tol32
     up.sync_status()
 
 
