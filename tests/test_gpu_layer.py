@@ -162,3 +162,32 @@ def test_llama_32k_sampled_rows(up):
         got = f64_of(Y[torch.as_tensor(rows, device="cuda")])
         assert rel(got, Yr) <= TOL
         assert np.abs(f64_of(lse)[:, rows] - lser).max() < LSE_TOL
+
+
+def _sampled_rows_check(up, name, sched, rows):
+    import torch
+    sh = SHAPES[name]
+    bits = layer_inputs(sh, 0)
+    dev = {k: to_dev(v) for k, v in bits.items() if k != "dY"}
+    s = up.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, sh.U, sh.C, sched)
+    Y, O, lse, st = up.attn_fwd(dev["X"], dev["W_qkv"], dev["W_o"], s)
+    torch.cuda.synchronize()
+    up.sync_status()
+    got = f64_of(Y[torch.as_tensor(rows, device="cuda")])
+    got_lse = f64_of(lse)[:, rows]
+    del Y, O, lse, dev
+    torch.cuda.empty_cache()
+    f = {k: bf16_bits_to_f64(bits[k]) for k in ("X", "W_qkv", "W_o")}
+    Yr, _, lser = orc.layer_forward_rows(f["X"], f["W_qkv"], f["W_o"], sh.H, sh.G, sh.d_head, rows)
+    assert rel(got, Yr) <= TOL
+    assert np.abs(got_lse - lser).max() < LSE_TOL
+
+
+def test_qwen3_32b_128k_sampled_rows(up):
+    """Qwen3-32B-shaped layer (S=131072, H=64, G=8, d_model=5120, U=8, C=8)."""
+    _sampled_rows_check(up, "qwen3_32b_128k", 0, np.array([0, 77, 4096, 65535, 100000, 131071]))
+
+
+def test_gqa_schedule_512k_sampled_rows(up):
+    """The GQA out-of-order schedule at S=524288 (Llama3-8B widths)."""
+    _sampled_rows_check(up, "llama3_8b_512k_gqa", 1, np.array([5, 262143, 524287]))
