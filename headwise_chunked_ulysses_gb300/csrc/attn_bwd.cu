@@ -14,15 +14,17 @@
 //   S^T = K Q^T, dP^T = V dO^T  (tensor cores -> TMEM)
 //   warps 4..11, two per TMEM lane quarter, each thread owning half of one
 //     KV row (64 query columns): P^T as bf16 back into S^T's TMEM columns,
-//     then dS^T = P^T * (dP^T - D) as bf16 into shared memory
-//   dV += P^T dO (A operand read from TMEM), dK += dS^T Q, dQ = dS K
-//     (tensor cores; dQ reuses dP's TMEM columns)
-//   the same warps, between P_{i+1} and dS_{i+1}, add dQ_i (half a query row
-//   per thread) into global memory with fp32 vector atomics.
-// MMA issue order dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}: the next scores are
-// computed while the softmax warps build dS_i.  The tensor pipe executes one
-// CTA's MMAs in issue order, so S_{i+1} overwrites P^T_i only after dV_i has
-// read it.
+//     then dS^T = P^T * (dP^T - D) as bf16 into the other half of those
+//     columns and into shared memory
+//   dV += P^T dO and dK += dS^T Q (A operands read from TMEM), dQ = dS K
+//     (both operands in shared memory; dQ reuses dP's TMEM columns)
+//   warps 12..15, one query row per thread, move dQ_i out of TMEM and add it
+//     into global memory with fp32 vector reductions.
+// MMA issue order dV_i, dQ_i, dK_i, S_{i+1}, dP_{i+1}: dQ_i is drained while
+// dK_i and S_{i+1} run, and dP_{i+1} waits only for dQ_i to have left TMEM.
+// The tensor pipe executes one CTA's MMAs in issue order, so S_{i+1}
+// overwrites P^T_i and dS^T_i only after dV_i and dK_i have read them.
+
 #include <cmath>
 
 #include "ptx.cuh"
@@ -61,7 +63,8 @@ struct BwdCfg {
   static constexpr int DS_OFF = LSE_OFF + 2 * BQ * 4;     // 2 stages x 128 fp32
   static constexpr int BAR_OFF = DS_OFF + 2 * BQ * 4;
   static constexpr int SMEM = BAR_OFF + 256;
-  // TMEM: S^T [0,128) (then P^T as bf16 pairs in [0,32) and [64,96))
+  // TMEM: S^T [0,128) (then P^T as bf16 pairs in [0,32) and [64,96), dS^T
+  //       in [32,64) and [96,128))
   //       dP^T / dQ [128,256)  dV [256,256+D)  dK [256+D,256+2D)
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
@@ -79,7 +82,7 @@ struct ItemCursor {
 };
 
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ BwdArgs a) {
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(ds_ready, 256);
     mbar_init(ds_consumed, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_drained, 256);
+    mbar_init(dq_drained, 128);
     mbar_init(kv_done, 1);
     *abort_flag = aligned ? 0 : 1;
     if (!aligned && a.status) atomicCAS(a.status, 0, kDevBadSmem);
@@ -208,30 +211,32 @@ __global__ void __launch_bounds__(384, 1)
             mma_ts(tmem + C::T_DV, tmem + C::T_S + (k >> 2) * 64 + (k & 3) * 8, sdesc_advance(b0, k * 2048), ID_KV,
                    (i | k) != 0);
         }
-        // next S^T: issued after dV_i, so it overwrites P^T_i only once dV_i has read it
+        // dQ = dS K (into dP's columns, read already), then dK += dS^T Q with
+        // dS^T read from TMEM: the softmax warps start draining dQ while dK runs
+        if (!mbar_wait(ds_ready, i & 1, w, 45)) break;
+        tc_fence_after();
+        {
+          const uint64_t a1 = sdesc_mnmajor(sDS, CH), b1 = sdesc_mnmajor(sK, CH);
+#pragma unroll
+          for (int k = 0; k < BKV / 16; ++k)
+            mma_ss(tmem + C::T_DP, sdesc_advance(a1, k * 2048), sdesc_advance(b1, k * 2048), ID_Q, k > 0);
+          mma_commit(dq_full);
+          mma_commit(ds_consumed);
+          const uint64_t b0 = sdesc_mnmajor(sQ(st), CH);
+#pragma unroll
+          for (int k = 0; k < BQ / 16; ++k)
+            mma_ts(tmem + C::T_DK, tmem + C::T_S + 32 + (k >> 2) * 64 + (k & 3) * 8, sdesc_advance(b0, k * 2048),
+                   ID_KV, (i | k) != 0);
+        }
+        mma_commit(&qdo_empty[st]);
+        // next S^T: issued after dV_i and dK_i, so it overwrites P^T_i and dS^T_i
+        // only once they have been read
         if (i + 1 < n_items) {
           if (!mbar_wait(&qdo_full[st ^ 1], ((i + 1) >> 1) & 1, w, 44)) break;
           tc_fence_after();
           qk_mma(tmem + C::T_S, sK, sQ(st ^ 1));
           mma_commit(s_full);
         }
-        // dK += dS^T Q ; dQ = dS K (into dP's columns, read already)
-        if (!mbar_wait(ds_ready, i & 1, w, 45)) break;
-        tc_fence_after();
-        {
-          const uint64_t a0 = sdesc_kmajor(sDS), b0 = sdesc_mnmajor(sQ(st), CH);
-#pragma unroll
-          for (int k = 0; k < BQ / 16; ++k)
-            mma_ss(tmem + C::T_DK, sdesc_advance(a0, (k >> 2) * CH + (k & 3) * 32), sdesc_advance(b0, k * 2048), ID_KV,
-                   (i | k) != 0);
-          const uint64_t a1 = sdesc_mnmajor(sDS, CH), b1 = sdesc_mnmajor(sK, CH);
-#pragma unroll
-          for (int k = 0; k < BKV / 16; ++k)
-            mma_ss(tmem + C::T_DP, sdesc_advance(a1, k * 2048), sdesc_advance(b1, k * 2048), ID_Q, k > 0);
-        }
-        mma_commit(ds_consumed);
-        mma_commit(dq_full);
-        mma_commit(&qdo_empty[st]);
         // next dP^T once dQ has been drained out of its columns
         if (i + 1 < n_items) {
           if (!mbar_wait(dq_drained, i & 1, w, 46)) break;
@@ -241,8 +246,8 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if (ok) mma_commit(kv_done);
-    } else if (warp >= 4) {
-      // ---------------- softmax, dS and dQ: half a row per thread ----------------
+    } else if (warp >= 4 && warp < 12) {
+      // ---------------- softmax and dS: half a row per thread ----------------
       const int q4 = warp & 3;
       const int half = (warp - 4) >> 2;  // 0: columns [0,64), 1: [64,128)
       const int row = q4 * 32 + lane;    // TMEM lane = KV row (S^T, dP^T) or query row (dQ)
@@ -250,33 +255,9 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
       const uint32_t sDS = smem_u32(smem + C::DS_TILE_OFF);
       const float sl2 = a.scale_log2;
-      ItemCursor cur, prev;
-      cur.kvb = prev.kvb = kvb;
-      cur.q_blocks = prev.q_blocks = a.q_blocks;
-      // dQ of the previous step (query row `row`, this thread's half of d) into global
-      auto drain_dq = [&](int i) -> bool {
-        if (!mbar_wait_warp(dq_full, i & 1, w, 53)) return false;
-        tc_fence_after();
-        const long long qrow = static_cast<long long>(prev.qs) * a.S + prev.qb * BQ + row;
-        // address of the 4 columns starting at column 4*g of query row qrow
-        auto col4 = [&](int g) -> float* {
-          return a.dq_tiled ? a.dQacc + ((qrow >> 5) * (D / 4) + g) * 128 + (qrow & 31) * 4
-                            : a.dQacc + qrow * D + 4 * g;
-        };
-#pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + C::T_DP + half * (D / 2) + c * 32, v);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            red_add_v4(col4((half * (D / 2) + c * 32) / 4 + e), __uint_as_float(v[4 * e]) * a.scale,
-                       __uint_as_float(v[4 * e + 1]) * a.scale, __uint_as_float(v[4 * e + 2]) * a.scale,
-                       __uint_as_float(v[4 * e + 3]) * a.scale);
-        }
-        tc_fence_before();
-        mbar_arrive(dq_drained);
-        return true;
-      };
+      ItemCursor cur;
+      cur.kvb = kvb;
+      cur.q_blocks = a.q_blocks;
       bool ok = true;
       int i = 0;
       for (; i < n_items && cur.next(a, kvs); ++i) {
@@ -309,11 +290,6 @@ __global__ void __launch_bounds__(384, 1)
         tmem_st32(tmem + lane_off + C::T_S + half * 64, pk);
         tc_fence_before();
         mbar_arrive(p_ready);
-        // dQ of the previous step, while the tensor cores run dV_i and S_{i+1}
-        if (i > 0) {
-          if (!drain_dq(i - 1)) { ok = false; break; }
-        }
-        prev = cur;
         // dS^T = P^T * (dP^T - D)
         if (!mbar_wait_warp(dp_full, i & 1, w, 50)) { ok = false; break; }
         tc_fence_after();
@@ -332,6 +308,9 @@ __global__ void __launch_bounds__(384, 1)
         }
         // the dS^T buffer is free once the previous step's dK and dQ MMAs are done
         if (i > 0 && !mbar_wait_warp(ds_consumed, (i - 1) & 1, w, 49)) { ok = false; break; }
+        // dS^T as bf16 pairs into the other 32 of this half's S^T columns (the A
+        // operand of dK), and into shared memory (the A operand of dQ)
+        tmem_st32(tmem + lane_off + C::T_S + half * 64 + 32, pk);
 #pragma unroll
         for (int piece = 0; piece < 8; ++piece)
           st_shared_v4(sDS + half * CH + row * 128 + ((piece ^ (row & 7)) << 4), pk[piece * 4], pk[piece * 4 + 1],
@@ -340,7 +319,6 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_before();
         mbar_arrive(ds_ready);
       }
-      if (ok && i > 0) ok = drain_dq(i - 1);
       // dK, dV epilogue: this thread's half of the d columns of KV row `row`
       if (ok && mbar_wait_warp(kv_done, 0, w, 52)) {
         tc_fence_after();
@@ -368,8 +346,41 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
+    } else if (warp >= 12) {
+      // ---------------- dQ: one query row per thread ----------------
+      // dQ_i leaves TMEM (freeing dP's columns for dP_{i+1}) and is added into
+      // the global fp32 accumulator with vector reductions, off the softmax
+      // warps' path
+      const int row = (warp & 3) * 32 + lane;
+      const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      ItemCursor cur;
+      cur.kvb = kvb;
+      cur.q_blocks = a.q_blocks;
+      for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
+        if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
+        tc_fence_after();
+        const long long qrow = static_cast<long long>(cur.qs) * a.S + cur.qb * BQ + row;
+        // address of the 4 columns starting at column 4*g of query row qrow
+        auto col4 = [&](int g) -> float* {
+          return a.dq_tiled ? a.dQacc + ((qrow >> 5) * (D / 4) + g) * 128 + (qrow & 31) * 4
+                            : a.dQacc + qrow * D + 4 * g;
+        };
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t v[64];
+          tmem_ld64(tmem + lane_off + C::T_DP + c * 64, v);
+          if (c == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(dq_drained);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            red_add_v4(col4(c * 16 + e), __uint_as_float(v[4 * e]) * a.scale, __uint_as_float(v[4 * e + 1]) * a.scale,
+                       __uint_as_float(v[4 * e + 2]) * a.scale, __uint_as_float(v[4 * e + 3]) * a.scale);
+        }
+      }
     }
-  } else if (aligned && n_items == 0 && !a.accumulate_kv && warp >= 4) {
+  } else if (aligned && n_items == 0 && !a.accumulate_kv && warp >= 4 && warp < 12) {
     // a KV slot no query head uses in this launch: its gradient is zero
     const int row = (warp & 3) * 32 + lane;
     const int half = (warp - 4) >> 2;
@@ -454,7 +465,7 @@ cudaError_t run_bwd(const CUtensorMap* tm, const BwdArgs& args, cudaStream_t st)
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<args.n_kvslots * args.q_blocks, 384, BwdCfg<D>::SMEM, st>>>(tm[0], tm[1], tm[2], tm[3], args);
+  kern<<<args.n_kvslots * args.q_blocks, 512, BwdCfg<D>::SMEM, st>>>(tm[0], tm[1], tm[2], tm[3], args);
   return cudaGetLastError();
 }
 
