@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
       const uint32_t sDS = smem_u32(smem + C::DS_TILE_OFF);
       const float sl2 = a.scale_log2;
+      const uint64_t sl2x2 = f2(sl2, sl2);
       ItemCursor cur;
       cur.kvb = kvb;
       cur.q_blocks = a.q_blocks;
@@ -276,8 +277,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int q0 = c * 32 + e;  // within this half
-            float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, -lse[q0]));
-            float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -lse[q0 + 1]));
+            const float2 l2 = *reinterpret_cast<const float2*>(lse + q0);
+            const uint64_t x = fma2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, f2(l2.x, l2.y));
+            float p0 = ex2(f2_lo(x));
+            float p1 = ex2(f2_hi(x));
             if (diag) {
               if (half * 64 + q0 < row) p0 = 0.f;
               if (half * 64 + q0 + 1 < row) p1 = 0.f;
@@ -301,9 +304,10 @@ __global__ void __launch_bounds__(512, 1)
           for (int e = 0; e < 32; e += 2) {
             const int q0 = c * 32 + e;
             const uint32_t pp = pk[q0 >> 1];
-            const float d0 = bf16_lo(pp) * (__uint_as_float(v[e]) - Dv[q0]);
-            const float d1 = bf16_hi(pp) * (__uint_as_float(v[e + 1]) - Dv[q0 + 1]);
-            pk[q0 >> 1] = pack_bf16(d0, d1);
+            const float2 d2 = *reinterpret_cast<const float2*>(Dv + q0);
+            const uint64_t ds = mul2(f2(bf16_lo(pp), bf16_hi(pp)),
+                                     sub2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), f2(d2.x, d2.y)));
+            pk[q0 >> 1] = pack_bf16(f2_lo(ds), f2_hi(ds));
           }
         }
         // the dS^T buffer is free once the previous step's dK and dQ MMAs are done
@@ -398,7 +402,8 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-// D = rowsum(dO * O) per (slot, token), lse in log2 units, dQ accumulator zeroed.
+// D = rowsum(dO * O) per (slot, token), minus lse in log2 units (the bias of the
+// exponent the backward recomputes P with), dQ accumulator zeroed.
 __global__ void bwd_prep_kernel(const BwdPrepDesc p) {
   const int lanes_per_row = p.D / 8;            // 16-byte vectors per row
   const int rows_per_warp = 32 / lanes_per_row;
@@ -426,7 +431,7 @@ __global__ void bwd_prep_kernel(const BwdPrepDesc p) {
   for (int off = lanes_per_row / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (r < total && v == 0) {
     p.Dsum[r] = acc;
-    p.lse2[r] = p.lse[static_cast<long long>(p.lse_row[slot]) * p.S + t] * 1.4426950408889634f;
+    p.lse2[r] = p.lse[static_cast<long long>(p.lse_row[slot]) * p.S + t] * -1.4426950408889634f;
   }
 }
 

@@ -8,11 +8,13 @@
 // One CTA per (query slot, 256 query rows) = two 128-row query tiles A and B
 // that take turns on the tensor cores; CTAs with the longest causal rows are
 // scheduled first.  TMEM (512 columns): S_A, S_B (128 fp32 columns each) and
-// O_A, O_B (d columns each).  Warp 0 streams 128-row K/V blocks by TMA into a
-// two-deep ring shared by both tiles; warp 1 issues, per KV block j,
+// O_A, O_B (d columns each).  Warp 0 streams 128-row K/V blocks by TMA into
+// two-deep rings shared by both tiles, K one block ahead of V (K_j is last read
+// by the scores of block j, V_j one step later by P V); warp 1 issues, per KV
+// block j,
 //   S_A(j) = Q_A K_j^T, S_B(j), then O_A += P_A(j) V_j, S_A(j+1), O_B += ...
 // Warps 4..7 (tile A) and 8..11 (tile B) own one query row per thread: they
-// read the row of S from TMEM, keep a per-row reference maximum (rescaling the
+// read the row of S from TMEM with one load, keep a per-row reference maximum (rescaling the
 // TMEM accumulator O only when the running maximum grows by more than 2^8,
 // which is exact since the same reference enters numerator and denominator),
 // and write P as bf16 pairs back into the first 64 columns of their S, where
@@ -68,11 +70,12 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;    // [2]
   uint64_t* v_full = bars + 3;    // [2]
-  uint64_t* kv_empty = bars + 5;  // [2]
+  uint64_t* k_empty = bars + 5;   // [2]
   uint64_t* s_full = bars + 7;    // [2] per tile
   uint64_t* p_ready = bars + 9;   // [2] per tile
   uint64_t* o_done = bars + 11;   // [2] per tile
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* v_empty = bars + 13;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -93,7 +96,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&p_ready[s], 128);
       mbar_init(&o_done[s], 1);
@@ -123,18 +127,25 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(smem + (tile ? C::QB_OFF : C::QA_OFF) + c * CH, &tmQ, q_full, c * 64,
                       slot * a.S + (tile ? qb1 : qb0) * BQ);
-      for (int j = 0; j < n_blocks; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1, w, 20)) break;
-        const int row = kvs * a.S + j * BKV;
-        mbar_arrive_expect_tx(&k_full[s], C::TILE);
+      // K of block j is last read by the scores of block j, one step before V of
+      // block j is last read by P V: K runs one block ahead of V
+      for (int j = 0; j <= n_blocks; ++j) {
+        if (j < n_blocks) {
+          const int s = j & 1;
+          if (!mbar_wait(&k_empty[s], ((j >> 1) & 1) ^ 1, w, 20)) break;
+          mbar_arrive_expect_tx(&k_full[s], C::TILE);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(smem + C::K_OFF + s * C::TILE + c * CH, &tmK, &k_full[s], c * 64, row);
-        mbar_arrive_expect_tx(&v_full[s], C::TILE);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(smem + C::K_OFF + s * C::TILE + c * CH, &tmK, &k_full[s], c * 64, kvs * a.S + j * BKV);
+        }
+        if (j > 0) {
+          const int jv = j - 1, s = jv & 1;
+          if (!mbar_wait(&v_empty[s], ((jv >> 1) & 1) ^ 1, w, 19)) break;
+          mbar_arrive_expect_tx(&v_full[s], C::TILE);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(smem + C::V_OFF + s * C::TILE + c * CH, &tmV, &v_full[s], c * 64, row);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(smem + C::V_OFF + s * C::TILE + c * CH, &tmV, &v_full[s], c * 64, kvs * a.S + jv * BKV);
+        }
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------- MMA issuer ----------------
@@ -168,6 +179,7 @@ __global__ void __launch_bounds__(384, 1)
       };
       if (ok) ok = issue_s(0, 0);
       if (ok && has_b) ok = issue_s(1, 0);
+      if (ok) mma_commit(&k_empty[0]);
       for (int j = 0; ok && j < n_blocks; ++j) {
         const int s = j & 1;
         if (j < n_kv0) {
@@ -186,7 +198,8 @@ __global__ void __launch_bounds__(384, 1)
             mma_commit(&o_done[1]);
           }
         }
-        mma_commit(&kv_empty[s]);
+        mma_commit(&v_empty[s]);
+        if (j + 1 < n_blocks) mma_commit(&k_empty[(j + 1) & 1]);
       }
     } else if (warp >= 4) {
       // ---------------- softmax: one query row of one tile per thread ----------------
@@ -206,20 +219,22 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           const bool diag = (j == nkv - 1);
           const int lim = diag ? qi - j * BKV : BKV;  // keys at column > lim are in the future
-          // pass 1: row maximum
+          // the whole row of S in one TMEM load: its maximum, then P from registers
+          uint32_t v[BKV];
+          tmem_ld128(t_s, v);
           float mx = -INFINITY;
+          if (diag) {
 #pragma unroll
-          for (int c = 0; c < BKV / 64; ++c) {
-            uint32_t v[64];
-            tmem_ld64(t_s + c * 64, v);
-            if (diag) {
+            for (int e = 0; e < BKV; ++e)
+              if (e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
+          } else {
+            float m4[4] = {mx, mx, mx, mx};
 #pragma unroll
-              for (int e = 0; e < 64; ++e)
-                if (c * 64 + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
-            } else {
+            for (int e = 0; e < BKV; e += 8) {
 #pragma unroll
-              for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+              for (int q = 0; q < 4; ++q) m4[q] = max3(m4[q], __uint_as_float(v[e + 2 * q]), __uint_as_float(v[e + 2 * q + 1]));
             }
+            mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           }
           const float m_new = fmaxf(m_run, mx * sl2);
           float alpha = 1.f;
@@ -229,49 +244,49 @@ __global__ void __launch_bounds__(384, 1)
             m_run = m_new;
             resc = true;
           }
-          // O (complete up to block j-1, see above) follows a raised reference
-          if (j > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t v[32];
-              tmem_ld32(t_o + c * 32, v);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-              tmem_st32(t_o + c * 32, v);
-            }
-          }
-          // pass 2: P = 2^(s*scale - m) as bf16 pairs into S's first 64 columns;
-          // 64 scores are read before the 32 columns holding their P are written
+          // P = 2^(s*scale - m) as bf16 pairs into S's first 64 columns (S itself
+          // is already in registers)
           float rs = 0.f;
+          uint64_t rs2 = f2(0.f, 0.f);
+          const uint64_t sl2x2 = f2(sl2, sl2), negm2 = f2(-m_run, -m_run);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t pk[32];
+            if (diag) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              uint32_t v[32];
-              tmem_ld32(t_s + h * 64 + c * 32, v);
-              if (diag) {
+              for (int e = 0; e < 64; e += 2) {
+                const int col = h * 64 + e;
+                const float p0 = col <= lim ? ex2(fmaf(__uint_as_float(v[col]), sl2, -m_run)) : 0.f;
+                const float p1 = col + 1 <= lim ? ex2(fmaf(__uint_as_float(v[col + 1]), sl2, -m_run)) : 0.f;
+                rs += p0 + p1;
+                pk[e >> 1] = pack_bf16(p0, p1);
+              }
+            } else {
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                  const int col = h * 64 + c * 32 + e;
-                  const float p0 = col <= lim ? ex2(fmaf(__uint_as_float(v[e]), sl2, -m_run)) : 0.f;
-                  const float p1 = col + 1 <= lim ? ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -m_run)) : 0.f;
-                  rs += p0 + p1;
-                  pk[c * 16 + (e >> 1)] = pack_bf16(p0, p1);
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                  const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, -m_run));
-                  const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -m_run));
-                  rs += p0 + p1;
-                  pk[c * 16 + (e >> 1)] = pack_bf16(p0, p1);
-                }
+              for (int e = 0; e < 64; e += 2) {
+                const int col = h * 64 + e;
+                const uint64_t x = fma2(f2(__uint_as_float(v[col]), __uint_as_float(v[col + 1])), sl2x2, negm2);
+                const float p0 = ex2(f2_lo(x));
+                const float p1 = ex2(f2_hi(x));
+                rs2 = add2(rs2, f2(p0, p1));
+                pk[e >> 1] = pack_bf16(p0, p1);
               }
             }
             tmem_st32(t_s + h * 32, pk);
           }
-          l_run = l_run * alpha + rs;
+          // O (complete up to block j-1, see above) follows a raised reference;
+          // done after P so that S no longer occupies registers
+          if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(t_o + c * 32, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(t_o + c * 32, o);
+            }
+          }
+          l_run = l_run * alpha + (rs + (f2_lo(rs2) + f2_hi(rs2)));
           tc_fence_before();
           mbar_arrive(&p_ready[tile]);
         }

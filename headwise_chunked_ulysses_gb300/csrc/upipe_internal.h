@@ -57,7 +57,7 @@ struct AttnBwdDesc {
   const void* K = nullptr;   // [n_kvslots][S][D] bf16
   const void* V = nullptr;   // [n_kvslots][S][D] bf16
   const void* dO = nullptr;  // [n_qslots][S][D] bf16
-  const float* lse2 = nullptr;  // [n_qslots][S]  log2-domain log-sum-exp
+  const float* lse2 = nullptr;  // [n_qslots][S]  minus the log-sum-exp in log2 units
   const float* Dsum = nullptr;  // [n_qslots][S]  rowsum(dO * O)
   float* dQacc = nullptr;    // fp32 per query slot, pre-zeroed, atomically accumulated
   // dQacc layout: 0 = [slot][S][D] row-major; 1 = tiled [slot][S/32][D/4][32][4]
@@ -99,7 +99,7 @@ struct BwdPrepDesc {
   const uint16_t* O = nullptr; long long ld_o = 0;    // seq layout (saved forward output)
   const float* lse = nullptr;                         // [*][S] natural log
   float* Dsum = nullptr;   // [n_slots][S]
-  float* lse2 = nullptr;   // [n_slots][S]
+  float* lse2 = nullptr;   // [n_slots][S]  -lse * log2(e)
   float* dQacc = nullptr;  // [n_slots][S][D], zeroed here
   int S = 0, D = 0, n_slots = 0;
   // slot -> start of its d-wide block, in units of D elements: a head index
