@@ -251,14 +251,16 @@ struct Cfg2 {
   static constexpr int B_BYTES = 128 * BK * 2;   // this CTA's B columns
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 512;          // two 256-column accumulators
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int EPI_OFF = STAGES * STAGE_BYTES;  // fp32 output staging: 4 warps x 2 x (32 x 32)
+  static constexpr int EPI_BYTES = 4 * 2 * 32 * 32 * 4;
+  static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
   static constexpr int SMEM = BAR_OFF + 256;
 };
 
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(256, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ GemmArgs g) {
+                 const __grid_constant__ CUtensorMap tmO, const __grid_constant__ GemmArgs g) {
   using C = Cfg2;
   constexpr int STAGES = C::STAGES;
   constexpr int BNP = 256;  // output columns per pair tile
@@ -372,8 +374,16 @@ __global__ void __launch_bounds__(256, 1)
       }
     } else if (warp >= 4) {
       // ---------------- epilogue: this CTA's 128 rows of the pair tile ----------------
+      // fp32 outputs leave through the TMA engine: each warp stages 32 x 32
+      // chunks of its rows (128-byte swizzle, two buffers) and stores them, or
+      // adds them atomically into the output (accumulate, split-K partials),
+      // with no read of the old values into the SM
       const int q = warp & 3;
       const int row = q * 32 + lane;
+      const bool tma_out = g.out_mode == kOutF32 || g.out_mode == kOutF32Acc || g.out_mode == kOutF32Red;
+      const bool tma_add = g.out_mode != kOutF32;
+      const uint32_t epi = smem_u32(smem + C::EPI_OFF) + q * (2 * 32 * 32 * 4);
+      int nb = 0;  // chunks this warp has handed to the TMA engine
       int tl = 0;
       for (int t = pair; t < n_tiles; t += n_pairs, ++tl) {
         const int acc = tl & 1;
@@ -387,11 +397,32 @@ __global__ void __launch_bounds__(256, 1)
           tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BNP + c * 32, v);
           const int n = n0 + c * 32;
           const int oc = g.use_omap_n ? g.omap_n[n >> 6] * 64 + (n & 63) : n;
-          store_tile_chunk(g, m, oc, v);
+          if (tma_out) {
+            const uint32_t buf = epi + (nb & 1) * (32 * 32 * 4);
+            if (nb >= 2) {  // the chunk sent two chunks ago has left this buffer
+              if (lane == 0) bulk_wait_read<1>();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+              st_shared_v4(buf + lane * 128 + ((p ^ (lane & 7)) << 4), v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (tma_add) tma_reduce_add_2d(&tmO, buf, oc, m - lane);
+              else tma_store_2d(&tmO, buf, oc, m - lane);
+              bulk_commit();
+            }
+            ++nb;
+          } else {
+            store_tile_chunk(g, m, oc, v);
+          }
         }
         tc_fence_before();
         mbar_arrive_remote(tempty0 + acc * 8);
       }
+      if (tma_out && lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   }
   tc_fence_before();
@@ -404,7 +435,8 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 template <bool A_MN, bool B_MN>
-cudaError_t run2(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, cudaStream_t st) {
+cudaError_t run2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const GemmArgs& args,
+                 cudaStream_t st) {
   auto kern = gemm2_kernel<A_MN, B_MN>;
   static bool configured = false;
   if (!configured) {
@@ -426,7 +458,7 @@ cudaError_t run2(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, to, args);
 }
 
 template <int BN, bool A_MN, bool B_MN>
@@ -482,10 +514,15 @@ cudaError_t launch_gemm(const GemmDesc& d, int* status, cudaStream_t st) {
   a.status = status;
   if (BN == 256 && d.M % 256 == 0 && num_sms() >= 2) {
     a.m_tiles = d.M / 256;  // pair tiles of 256 x 256
-    if (d.a_mn && d.b_mn) return run2<true, true>(ta, tb, a, st);
-    if (d.a_mn) return run2<true, false>(ta, tb, a, st);
-    if (d.b_mn) return run2<false, true>(ta, tb, a, st);
-    return run2<false, false>(ta, tb, a, st);
+    // fp32 outputs: a map over the whole output buffer, 32 x 32 boxes
+    CUtensorMap to = ta;
+    if ((d.out_mode == kOutF32 || d.out_mode == kOutF32Acc || d.out_mode == kOutF32Red) &&
+        !make_tmap_f32(&to, d.out, d.ldo, d.M, d.ldo, 32, 32))
+      return cudaErrorInvalidValue;
+    if (d.a_mn && d.b_mn) return run2<true, true>(ta, tb, to, a, st);
+    if (d.a_mn) return run2<true, false>(ta, tb, to, a, st);
+    if (d.b_mn) return run2<false, true>(ta, tb, to, a, st);
+    return run2<false, false>(ta, tb, to, a, st);
   }
   if (BN == 256) return dispatch_major<256>(d, ta, tb, a, st);
   if (BN == 128) return dispatch_major<128>(d, ta, tb, a, st);

@@ -121,6 +121,8 @@ cudaError_t launch_dq_tiled_to_seq(const DqTiledDesc& p, cudaStream_t st);
 // Tensor maps (driver entry point resolved through the runtime).
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
                     uint32_t box_inner, uint32_t box_outer);
+bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
+                   uint32_t box_inner, uint32_t box_outer);
 int num_sms();
 // Device address of the status word bounded waits write (read by upipe_sync_status).
 int* device_status_word();
