@@ -284,6 +284,10 @@ def run_sweep(args):
         Y, O, lse, _ = upipe.attn_fwd(X, Wqkv, Wo, s, ws=wsf)
         dX, dWqkv, dWo, _ = upipe.attn_bwd(X, Wqkv, Wo, O, lse, dY, s, ws=wsb)
         torch.cuda.synchronize()
+        clocks = ClockSampler(0)
+        clocks.start()
+        upipe.profile_enable(True)
+        upipe.profile_read()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(args.sweep_steps):
@@ -291,6 +295,9 @@ def run_sweep(args):
             _, _, _, stb = upipe.attn_bwd(X, Wqkv, Wo, O, lse, dY, s, dX=dX, dW_qkv=dWqkv, dW_o=dWo, ws=wsb)
         e1.record()
         torch.cuda.synchronize()
+        clk = clocks.stop()
+        prof = upipe.profile_read()
+        upipe.profile_enable(False)
         upipe.sync_status()
         ms = e0.elapsed_time(e1) / args.sweep_steps
         tf = model_flops_step(sh) / (ms / 1e3) / 1e12
@@ -302,7 +309,8 @@ def run_sweep(args):
             "closed_form_12SUd": stf["stage_closed_form_bytes"],
             "ulysses_form_12SHd": 12 * sh.S * sh.H * sh.d_head,
             "permute_bytes_fwd": stf["permute_bytes"], "permute_bytes_bwd": stb["permute_bytes"],
-            "persistent_bytes": stf["persistent_bytes"], "steps": args.sweep_steps}), flush=True)
+            "persistent_bytes": stf["persistent_bytes"], "steps": args.sweep_steps, "clocks": clk,
+            "kernel_ms_per_step": {k: v[0] / args.sweep_steps for k, v in prof.items()}}), flush=True)
         del X, dY, Wqkv, Wo, wsf, wsb, Y, O, lse, dX, dWqkv, dWo
         torch.cuda.empty_cache()
     return 0
@@ -454,25 +462,67 @@ def main():
         h2d = sum(v.numel() * v.element_size() for v in pin.values())
         d2h = sum(v.numel() * v.element_size() for v in outs.values())
 
-        def e2e_step():
-            for k in pin:
-                d[k].copy_(pin[k], non_blocking=True)
-            step()
-            outs["Y"].copy_(Y, non_blocking=True)
-            outs["dX"].copy_(dX, non_blocking=True)
-            outs["dW_qkv"].copy_(dWqkv, non_blocking=True)
-            outs["dW_o"].copy_(dWo, non_blocking=True)
-        e2e_step()
+        # Every step copies its inputs in from pinned host memory and its
+        # results back out, all inside the timed region.  The copies run on
+        # two copy streams (one per direction), double-buffered on the device,
+        # so step k+1's inputs arrive and step k's results leave while step k
+        # (resp. k+1) computes -- the way a training loop feeds the layer.
+        h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        din = [d, {k: torch.empty_like(v) for k, v in d.items()}]
+        dout = [{"Y": Y, "dX": dX, "dW_qkv": dWqkv, "dW_o": dWo},
+                {"Y": torch.empty_like(Y), "dX": torch.empty_like(dX), "dW_qkv": torch.empty_like(dWqkv),
+                 "dW_o": torch.empty_like(dWo)}]
+        hout = [outs, {k: torch.empty_like(v).pin_memory() for k, v in outs.items()}]
+
+        def run_e2e(n):
+            ev = lambda: torch.cuda.Event()
+            in_ready, in_free, out_ready, out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()], [ev(), ev()]
+            start = ev()
+            start.record(stream)
+            h2d_s.wait_event(start)
+            with torch.cuda.stream(h2d_s):
+                for k in din[0]:
+                    din[0][k].copy_(pin[k], non_blocking=True)
+            in_ready[0].record(h2d_s)
+            for i in range(n):
+                b = i & 1
+                if i + 1 < n:  # inputs of step i+1, once step i-1 has finished with that buffer
+                    nb = b ^ 1
+                    if i >= 1:
+                        h2d_s.wait_event(in_free[nb])
+                    with torch.cuda.stream(h2d_s):
+                        for k in din[nb]:
+                            din[nb][k].copy_(pin[k], non_blocking=True)
+                    in_ready[nb].record(h2d_s)
+                stream.wait_event(in_ready[b])
+                if i >= 2:
+                    stream.wait_event(out_free[b])
+                o = dout[b]
+                upipe.attn_fwd(din[b]["X"], din[b]["W_qkv"], din[b]["W_o"], s, Y=o["Y"], O_saved=O, lse=lse, ws=wsf)
+                upipe.attn_bwd(din[b]["X"], din[b]["W_qkv"], din[b]["W_o"], O, lse, din[b]["dY"], s, dX=o["dX"],
+                               dW_qkv=o["dW_qkv"], dW_o=o["dW_o"], ws=wsb)
+                in_free[b].record(stream)
+                out_ready[b].record(stream)
+                d2h_s.wait_event(out_ready[b])
+                with torch.cuda.stream(d2h_s):
+                    for k in hout[b]:
+                        hout[b][k].copy_(o[k], non_blocking=True)
+                out_free[b].record(d2h_s)
+            stream.wait_stream(d2h_s)
+            stream.wait_stream(h2d_s)
+
+        run_e2e(2)
         barrier()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        run_e2e(args.steps)
         f1.record(stream)
         barrier()
         e_ms = max_over_ranks(f0.elapsed_time(f1), dev)
         e2e = {"value": aggregate_tokens_per_s(world, sh.S, args.steps, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps,
+               "copies": "per step: all inputs host->device and Y, dX, dW_qkv, dW_o device->host, on two copy "
+                         "streams overlapping the neighbouring steps' compute (double-buffered on the device)"}
         upipe.sync_status()
 
     mem_peak = torch.cuda.max_memory_allocated(dev) - mem_before

@@ -25,6 +25,7 @@
 // The tensor pipe executes one CTA's MMAs in issue order, so S_{i+1}
 // overwrites P^T_i and dS^T_i only after dV_i and dK_i have read them.
 
+#include <algorithm>
 #include <cmath>
 
 #include "ptx.cuh"
@@ -42,6 +43,7 @@ struct BwdArgs {
   float scale_log2, scale;
   int accumulate_kv;
   int dq_tiled;
+  int grp_slots;  // KV slots per group of the CTA order (divides n_kvslots)
   uint16_t kv_slot[kMaxSlots];
   const float* lse2;
   const float* Dsum;
@@ -109,8 +111,14 @@ __global__ void __launch_bounds__(512, 1)
   const Watch w{abort_flag, a.status};
   const bool aligned = (smem_u32(smem) & 1023u) == 0;
 
-  const int kvb = static_cast<int>(blockIdx.x) / a.n_kvslots;  // block 0 (most work) first
-  const int kvs = static_cast<int>(blockIdx.x) % a.n_kvslots;
+  // CTA order: KV slots in groups of grp_slots, and within a group block 0
+  // (most work) first, so the CTAs running at one time share few slots'
+  // query-side data
+  const int grp_slots = a.grp_slots;
+  const int per_grp = grp_slots * a.q_blocks;
+  const int grp = static_cast<int>(blockIdx.x) / per_grp, rem = static_cast<int>(blockIdx.x) % per_grp;
+  const int kvb = rem / grp_slots;
+  const int kvs = grp * grp_slots + rem % grp_slots;
   int n_q = 0;
   for (int i = 0; i < a.n_qslots; ++i) n_q += (a.kv_slot[i] == kvs);
   const int n_items = n_q * (a.q_blocks - kvb);
@@ -510,6 +518,12 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) 
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.D)));
   a.accumulate_kv = d.accumulate_kv;
   a.dq_tiled = d.dq_tiled;
+  // at most 2^20 tokens of query-side data per group of concurrently running
+  // slots (8 slots up to S = 128K, fewer beyond), a divisor of n_kvslots
+  int g = std::max(1, std::min(8, (1 << 20) / d.S));
+  g = std::min(g, d.n_kvslots);
+  while (g > 1 && d.n_kvslots % g) --g;
+  a.grp_slots = g;
   for (int i = 0; i < d.n_qslots; ++i) a.kv_slot[i] = d.kv_slot[i];
   a.lse2 = d.lse2;
   a.Dsum = d.Dsum;

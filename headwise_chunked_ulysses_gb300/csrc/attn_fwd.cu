@@ -82,9 +82,14 @@ __global__ void __launch_bounds__(384, 1)
   const Watch w{abort_flag, a.status};
   const bool aligned = (smem_u32(smem) & 1023u) == 0;
 
-  // longest causal rows first: pair index t covers query blocks 2t and 2t+1
-  const int t = a.q_pairs - 1 - static_cast<int>(blockIdx.x) / a.n_qslots;
-  const int slot = static_cast<int>(blockIdx.x) % a.n_qslots;
+  // longest causal rows first: pair index t covers query blocks 2t and 2t+1;
+  // more than 8 query slots go in groups of 8 (each group longest first), so
+  // the CTAs running at one time share few slots' K/V
+  const int grp_slots = (a.n_qslots > 8 && a.n_qslots % 8 == 0) ? 8 : a.n_qslots;
+  const int per_grp = grp_slots * a.q_pairs;
+  const int grp = static_cast<int>(blockIdx.x) / per_grp, rem = static_cast<int>(blockIdx.x) % per_grp;
+  const int t = a.q_pairs - 1 - rem / grp_slots;
+  const int slot = grp * grp_slots + rem % grp_slots;
   const int kvs = a.kv_slot[slot];
   const int qb0 = 2 * t, qb1 = 2 * t + 1;
   const bool has_b = qb1 < a.q_blocks;

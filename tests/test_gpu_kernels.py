@@ -104,7 +104,9 @@ def _attn_inputs(n_q, n_kv, S, d, seed):
 
 
 CASES = [(4, 2, 384, 64, [0, 0, 1, 1]), (4, 2, 256, 128, [0, 0, 1, 1]), (2, 2, 1024, 128, [0, 1]),
-         (3, 1, 128, 64, [0, 0, 0]), (2, 4, 512, 64, [3, 1])]
+         (3, 1, 128, 64, [0, 0, 0]), (2, 4, 512, 64, [3, 1]),
+         # more than 8 slots: the kernels order their CTAs in groups of 8 slots
+         (16, 16, 512, 128, list(range(16))), (16, 8, 384, 64, [k // 2 for k in range(16)])]
 
 
 @pytest.mark.parametrize("n_q,n_kv,S,d,kv", CASES)
