@@ -223,7 +223,7 @@ void build_schedule(Plan& p) {
 
 // Workspace: [stage arena | persistent].  The stage arena holds the sequence-
 // layout stage buffer (QKV, then reused for dO and dQKV) and the head-layout
-// exchange buffers; the persistent part holds the backward's fp32 dX accumulator.
+// exchange buffers; the persistent part holds the fp32 Y / dX accumulator.
 Plan make_plan(const Shape& s, bool backward) {
   Plan p;
   p.sh = s;
@@ -245,7 +245,7 @@ Plan make_plan(const Shape& s, bool backward) {
     o = align256(o + (U + 2 * p.n_kv_slots) * S * d * 4);
   }
   p.arena = o;
-  const int acc_gemms = backward ? p.n_stages + (s.sched == UPIPE_SCHED_GQA_OOO ? 1 : 0) : 1;
+  const int acc_gemms = backward ? p.n_stages + (s.sched == UPIPE_SCHED_GQA_OOO ? 1 : 0) : p.n_stages;
   p.off_acc32 = o;
   if (acc_gemms > 1) o = align256(o + S * s.dm * 4);
   p.persistent = o - p.arena;
@@ -468,6 +468,7 @@ int upipe_attn_fwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
   const int d = d_head;
   uint16_t* qkvh = reinterpret_cast<uint16_t*>(w + p.off_qkvh);
   uint16_t* oh = reinterpret_cast<uint16_t*>(w + p.off_seq);  // the sequence buffer is dead after the exchange
+  float* y32 = reinterpret_cast<float*>(w + p.off_acc32);
   const size_t slot_elems = static_cast<size_t>(S) * d;
   for (int i = 0; i < p.n_stages && L.ok(); ++i) {
     const Stage& g = p.st[i];
@@ -497,15 +498,24 @@ int upipe_attn_fwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
       b.src_slot[k] = static_cast<uint16_t>(k);
     }
     L.h2s(b);
-  }
-  // output projection Y = O W_o, once O_saved holds every head (the same sum
-  // over heads as adding each stage's share, in one GEMM with K = H d_head)
-  if (L.ok()) {
+    // (5) the stage's heads' share of the output projection accumulates into Y:
+    // fp32 Y32 = O_s W_o[rows of s] for the first stage, += for the next ones
+    // (TMA stores / atomic adds), bf16 Y = Y32 + the last share
     GemmDesc go;
     go.A = O_saved; go.lda = static_cast<long long>(H) * d; go.a_rows = S; go.a_cols = go.lda; go.a_mn = false;
     go.B = W_o; go.ldb = d_model; go.b_rows = static_cast<long long>(H) * d; go.b_cols = d_model; go.b_mn = true;
-    go.M = S; go.N = d_model; go.K = H * d;
-    go.out = Y; go.ldo = d_model; go.out_mode = kOutBf16;
+    go.M = S; go.N = d_model; go.K = U * d;
+    head_blocks(go.amap_k, g.q_heads, d);
+    go.bmap_k = go.amap_k;
+    if (p.n_stages == 1) {
+      go.out = Y; go.ldo = d_model; go.out_mode = kOutBf16;
+    } else if (i == 0) {
+      go.out = y32; go.ldo = d_model; go.out_mode = kOutF32;
+    } else if (i + 1 < p.n_stages) {
+      go.out = y32; go.ldo = d_model; go.out_mode = kOutF32Acc;
+    } else {
+      go.out = Y; go.ldo = d_model; go.out_mode = kOutBf16PlusF32; go.aux = y32; go.ld_aux = d_model;
+    }
     L.gemm(go);
   }
   return finish(L, p, stats);

@@ -9,8 +9,8 @@
  *   - Method steps (1)-(4): per stage, project X onto the Q, K, V of heads
  *     iU..(i+1)U-1; all-to-all from sequence shards (S/C tokens per rank) to
  *     head shards (U/C heads of all S tokens per rank); causal attention;
- *     all-to-all back.  The output projection Y = O W_o follows once O holds
- *     every head (the pages stop at the output all-to-all).
+ *     all-to-all back.  Each stage then adds its heads' share of the output
+ *     projection, O_s W_o[rows of s], into Y.
  *   - Novelty: the GQA schedule takes heads out of order so every KV head is
  *     exchanged once, in the first stage, and later stages move query heads only.
  *   - Background: DeepSpeed Ulysses (the all-to-all) and GQA (H query heads
@@ -98,8 +98,8 @@ size_t upipe_fwd_workspace_bytes(int S, int d_model, int H, int G, int d_head, i
 size_t upipe_bwd_workspace_bytes(int S, int d_model, int H, int G, int d_head, int U, int C, int sched);
 
 /*
- * Forward pass of the layer (Method steps (1)-(4) per stage, then the output
- * projection Y = O W_o).
+ * Forward pass of the layer (Method steps (1)-(4) per stage, plus the
+ * stage's share of Y = O W_o).
  *   X, W_qkv, W_o : device, bf16, inputs.
  *   Y             : device, bf16 [S, d_model], output.
  *   O_saved       : device, bf16 [S, H*d_head], output (attention output of every
