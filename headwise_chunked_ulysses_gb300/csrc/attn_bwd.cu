@@ -283,17 +283,20 @@ __global__ void __launch_bounds__(512, 1)
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + C::T_S + half * 64 + c * 32, v);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
+          for (int e = 0; e < 32; e += 4) {
             const int q0 = c * 32 + e;  // within this half
-            const float2 l2 = *reinterpret_cast<const float2*>(lse + q0);
-            const uint64_t x = fma2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, f2(l2.x, l2.y));
-            float p0 = ex2(f2_lo(x));
-            float p1 = ex2(f2_hi(x));
+            const float4 l4 = *reinterpret_cast<const float4*>(lse + q0);
+            const uint64_t xa = fma2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, f2(l4.x, l4.y));
+            const uint64_t xb = fma2(f2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), sl2x2, f2(l4.z, l4.w));
+            float p0 = ex2(f2_lo(xa)), p1 = ex2(f2_hi(xa)), p2 = ex2(f2_lo(xb)), p3 = ex2(f2_hi(xb));
             if (diag) {
               if (half * 64 + q0 < row) p0 = 0.f;
               if (half * 64 + q0 + 1 < row) p1 = 0.f;
+              if (half * 64 + q0 + 2 < row) p2 = 0.f;
+              if (half * 64 + q0 + 3 < row) p3 = 0.f;
             }
             pk[q0 >> 1] = pack_bf16(p0, p1);
+            pk[(q0 >> 1) + 1] = pack_bf16(p2, p3);
           }
         }
         // P^T (bf16 pairs) into the first 32 columns of this half's own S^T
@@ -309,13 +312,16 @@ __global__ void __launch_bounds__(512, 1)
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + C::T_DP + half * 64 + c * 32, v);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
+          for (int e = 0; e < 32; e += 4) {
             const int q0 = c * 32 + e;
-            const uint32_t pp = pk[q0 >> 1];
-            const float2 d2 = *reinterpret_cast<const float2*>(Dv + q0);
-            const uint64_t ds = mul2(f2(bf16_lo(pp), bf16_hi(pp)),
-                                     sub2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), f2(d2.x, d2.y)));
-            pk[q0 >> 1] = pack_bf16(f2_lo(ds), f2_hi(ds));
+            const float4 d4 = *reinterpret_cast<const float4*>(Dv + q0);
+            const uint32_t pa = pk[q0 >> 1], pb = pk[(q0 >> 1) + 1];
+            const uint64_t da = mul2(f2(bf16_lo(pa), bf16_hi(pa)),
+                                     sub2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), f2(d4.x, d4.y)));
+            const uint64_t db = mul2(f2(bf16_lo(pb), bf16_hi(pb)),
+                                     sub2(f2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), f2(d4.z, d4.w)));
+            pk[q0 >> 1] = pack_bf16(f2_lo(da), f2_hi(da));
+            pk[(q0 >> 1) + 1] = pack_bf16(f2_lo(db), f2_hi(db));
           }
         }
         // the dS^T buffer is free once the previous step's dK and dQ MMAs are done
