@@ -269,7 +269,8 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;  // used in CTA 0
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* aux_full = tempty + 2;  // [4 warps][2 buffers]: accumulator chunks loaded for bf16 = acc + aux
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_full + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -286,6 +287,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 256);  // both CTAs' epilogue threads
     }
+    for (int b = 0; b < 8; ++b) mbar_init(&aux_full[b], 1);
     *abort_flag = aligned ? 0 : 1;
     if (!aligned && g.status) atomicCAS(g.status, 0, kDevBadSmem);
     fence_mbar_init();
@@ -382,8 +384,11 @@ __global__ void __launch_bounds__(256, 1)
       const int row = q * 32 + lane;
       const bool tma_out = g.out_mode == kOutF32 || g.out_mode == kOutF32Acc || g.out_mode == kOutF32Red;
       const bool tma_add = g.out_mode != kOutF32;
+      // bf16 = acc + aux: the aux (fp32) chunks come in by TMA, one ahead
+      const bool aux_in = g.out_mode == kOutBf16PlusF32;
       const uint32_t epi = smem_u32(smem + C::EPI_OFF) + q * (2 * 32 * 32 * 4);
-      int nb = 0;  // chunks this warp has handed to the TMA engine
+      uint64_t* abar = aux_full + q * 2;
+      int nb = 0;  // chunks this warp has handed to (or taken from) the TMA engine
       int tl = 0;
       for (int t = pair; t < n_tiles; t += n_pairs, ++tl) {
         const int acc = tl & 1;
@@ -391,12 +396,24 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         const int m = tile_m0(t) + 128 * static_cast<int>(rank) + row;
         const int n0 = tile_n0(t);
+        auto out_col = [&](int c) {
+          const int n = n0 + c * 32;
+          return g.use_omap_n ? g.omap_n[n >> 6] * 64 + (n & 63) : n;
+        };
+        auto load_aux = [&](int c, int k) {  // chunk c of this warp's rows into buffer k&1
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&abar[k & 1], 32 * 32 * 4);
+            tma_load_2d(smem + C::EPI_OFF + q * (2 * 32 * 32 * 4) + (k & 1) * (32 * 32 * 4), &tmO, &abar[k & 1],
+                        out_col(c), m - lane);
+          }
+        };
+        if (aux_in) load_aux(0, nb);
+        bool ok = true;
 #pragma unroll 1
         for (int c = 0; c < BNP / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BNP + c * 32, v);
-          const int n = n0 + c * 32;
-          const int oc = g.use_omap_n ? g.omap_n[n >> 6] * 64 + (n & 63) : n;
+          const int oc = out_col(c);
           if (tma_out) {
             const uint32_t buf = epi + (nb & 1) * (32 * 32 * 4);
             if (nb >= 2) {  // the chunk sent two chunks ago has left this buffer
@@ -414,10 +431,30 @@ __global__ void __launch_bounds__(256, 1)
               bulk_commit();
             }
             ++nb;
+          } else if (aux_in) {
+            // the next chunk's aux is on its way while this one is added
+            if (c + 1 < BNP / 32) load_aux(c + 1, nb + 1);
+            if (!mbar_wait_warp(&abar[nb & 1], (nb >> 1) & 1, w, 65)) { ok = false; break; }
+            const uint32_t buf = epi + (nb & 1) * (32 * 32 * 4);
+            uint32_t pk16[16];
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+              const uint4 x = ld_shared_v4(buf + lane * 128 + ((p ^ (lane & 7)) << 4));
+              pk16[2 * p] = pack_bf16(__uint_as_float(v[4 * p]) + __uint_as_float(x.x),
+                                      __uint_as_float(v[4 * p + 1]) + __uint_as_float(x.y));
+              pk16[2 * p + 1] = pack_bf16(__uint_as_float(v[4 * p + 2]) + __uint_as_float(x.z),
+                                          __uint_as_float(v[4 * p + 3]) + __uint_as_float(x.w));
+            }
+            __syncwarp();  // every lane has read the buffer before it is loaded again
+            uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(g.out) + (long long)m * g.ldo + oc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk16[4 * i], pk16[4 * i + 1], pk16[4 * i + 2], pk16[4 * i + 3]);
+            ++nb;
           } else {
             store_tile_chunk(g, m, oc, v);
           }
         }
+        if (!ok) break;
         tc_fence_before();
         mbar_arrive_remote(tempty0 + acc * 8);
       }
@@ -518,6 +555,9 @@ cudaError_t launch_gemm(const GemmDesc& d, int* status, cudaStream_t st) {
     CUtensorMap to = ta;
     if ((d.out_mode == kOutF32 || d.out_mode == kOutF32Acc || d.out_mode == kOutF32Red) &&
         !make_tmap_f32(&to, d.out, d.ldo, d.M, d.ldo, 32, 32))
+      return cudaErrorInvalidValue;
+    // bf16 = acc + aux: the map reads the fp32 aux in 32 x 32 boxes
+    if (d.out_mode == kOutBf16PlusF32 && !make_tmap_f32(&to, d.aux, d.ld_aux, d.M, d.ld_aux, 32, 32))
       return cudaErrorInvalidValue;
     if (d.a_mn && d.b_mn) return run2<true, true>(ta, tb, to, a, st);
     if (d.a_mn) return run2<true, false>(ta, tb, to, a, st);
