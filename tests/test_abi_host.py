@@ -99,6 +99,28 @@ def test_backward_arena_has_no_h_term(upipe):
             assert b64 - b32 <= 8 * S * d * 16 + 4096
 
 
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b_32k", "qwen3_32b_128k", "llama3_8b_256k_usweep"])
+@pytest.mark.parametrize("U", [None, "H"])
+def test_backward_arena_follows_its_closed_form(upipe, name, U):
+    """In order: the sequence-layout stage buffer (the stage's Q heads and the
+    KV heads they use, 2 bytes), the head-layout Q and per-slot K, V (6 bytes
+    per slot element), dO in head layout (2), D and lse (4 + 4 per slot and
+    token) and the fp32 dQ, dK, dV slots (12): (22 + 4 G/H) S U d + 8 S U bytes
+    when U >= H/G (with one KV head per stage otherwise), up to 256-byte
+    alignment of the 7 buffers."""
+    from synthetic import SHAPES
+    s = SHAPES[name]
+    u = s.H if U == "H" else s.U
+    sh = upipe.Shape(s.S, s.d_model, s.H, s.G, s.d_head, u, s.C, upipe.IN_ORDER)
+    stages = s.H // u
+    arena = upipe.bwd_workspace_bytes(sh) - (s.S * s.d_model * 4 if stages > 1 else 0)
+    kv = max(1, u * s.G // s.H)  # KV heads a stage's contiguous query heads use
+    form = 2 * s.S * s.d_head * (u + 2 * kv) + (6 + 2 + 12) * s.S * u * s.d_head + 8 * s.S * u
+    if u * s.G >= s.H:
+        assert form == (22 * s.S * u * s.d_head + 4 * s.S * u * s.d_head * s.G // s.H + 8 * s.S * u)
+    assert 0 <= arena - form <= 7 * 256
+
+
 def test_invalid_shapes_are_rejected(upipe):
     bad = [
         upipe.Shape(1024, 512, 8, 2, 64, 3, 1),     # U does not divide H
