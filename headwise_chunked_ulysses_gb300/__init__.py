@@ -23,7 +23,7 @@ OK, EINVAL, ENOSPC, EUNSUPPORTED, ECUDA, ETIMEOUT = range(6)
 # Entry points declared in include/upipe.h
 EXPORTS = (
     "upipe_fwd_workspace_bytes", "upipe_bwd_workspace_bytes", "upipe_attn_fwd", "upipe_attn_bwd",
-    "upipe_layout_seq2head", "upipe_layout_head2seq", "upipe_schedule_table",
+    "upipe_layout_seq2head", "upipe_layout_head2seq", "upipe_schedule_table", "upipe_choose_u",
     "upipe_attention_fwd", "upipe_attention_bwd", "upipe_attention_bwd_noalloc", "upipe_gemm_bf16",
     "upipe_sync_status", "upipe_status_str", "upipe_version", "upipe_profile_enable", "upipe_profile_read",
 )
@@ -68,6 +68,7 @@ def _sig(lib):
         "upipe_layout_seq2head": (I, [P, P, I, I, I, I, I, P]),
         "upipe_layout_head2seq": (I, [P, P, I, I, I, I, I, P]),
         "upipe_schedule_table": (I, [I, I, I, I, I, i32p]),
+        "upipe_choose_u": (I, [I, I, I, I, I, I, I, Z]),
         "upipe_attention_fwd": (I, [P, P, P, I, I, I, I, i32p, P, P, P]),
         "upipe_attention_bwd": (I, [P, P, P, P, P, P, I, I, I, I, i32p, P, P, P, P, Z, P]),
         "upipe_attention_bwd_noalloc": (I, [P, P, P, P, P, P, I, I, I, I, i32p, P, P, P, P]),
@@ -152,6 +153,12 @@ def schedule_table(H, G, U, C, sched=IN_ORDER):
     _check("upipe_schedule_table", lib().upipe_schedule_table(
         H, G, U, C, sched, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
     return out.reshape(H // U, C, U // C)
+
+
+def choose_u(S, d_model, H, G, d_head, C, sched, budget_bytes):
+    """Largest stage width U whose forward and backward workspaces fit in
+    budget_bytes (0 if none does); see upipe_choose_u."""
+    return int(lib().upipe_choose_u(S, d_model, H, G, d_head, C, sched, int(budget_bytes)))
 
 
 def _workspace(nbytes, device):

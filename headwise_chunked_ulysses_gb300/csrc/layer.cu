@@ -732,6 +732,17 @@ int upipe_schedule_table(int H, int G, int U, int C, int sched, int32_t* host_ou
   return UPIPE_OK;
 }
 
+int upipe_choose_u(int S, int d_model, int H, int G, int d_head, int C, int sched, size_t budget_bytes) {
+  int best = 0;
+  for (int U = 1; U <= H; ++U) {
+    const Shape s{S, d_model, H, G, d_head, U, C, sched};
+    if (check_shape(s) != UPIPE_OK) continue;
+    const size_t need = std::max(make_plan(s, false).total, make_plan(s, true).total);
+    if (need <= budget_bytes) best = U;
+  }
+  return best;
+}
+
 int upipe_attention_fwd(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf16* V, int n_q, int n_kv, int S,
                         int d_head, const int32_t* kv_of_q, upipe_bf16* O, float* lse, void* stream) {
   const void* ptrs[] = {Q, K, V, O, lse};

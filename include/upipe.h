@@ -152,6 +152,18 @@ int upipe_layout_head2seq(const upipe_bf16* src, upipe_bf16* dst, int S, int n_h
 int upipe_schedule_table(int H, int G, int U, int C, int sched, int32_t* host_out);
 
 /*
+ * Stage width chooser ("Untied Ulysses" summary, paper.rainbus.top, section
+ * on weaknesses from an independent analysis: pick U from the sequence length,
+ * large U for short sequences to save launches, small U for long ones to save
+ * memory).  Returns the largest U (U | H, C | U, and the schedule's own
+ * constraints; U = H is plain Ulysses) for which both
+ * upipe_fwd_workspace_bytes() and upipe_bwd_workspace_bytes() are at most
+ * budget_bytes, or 0 if no valid U fits or the shape is invalid for every U.
+ * Host only: touches no device and allocates nothing.
+ */
+int upipe_choose_u(int S, int d_model, int H, int G, int d_head, int C, int sched, size_t budget_bytes);
+
+/*
  * Causal GQA attention of one stage's heads in head layout (Method steps (3)).
  *   Q   : device bf16 [n_q][S][d_head];  K, V: device bf16 [n_kv][S][d_head].
  *   kv_of_q : HOST int32 [n_q], the KV slot each query slot reads.

@@ -156,3 +156,40 @@ def test_arguments_checked_before_any_launch(upipe):
     rc = lib.upipe_layout_seq2head(fake, fake, 1024, 6, 64, 4, 384, None)
     assert rc == upipe.EINVAL
     assert lib.upipe_status_str(upipe.ETIMEOUT) == b"a kernel wait timed out"
+
+
+def _valid_us(upipe, S, dm, H, G, d, C, sched):
+    return [U for U in range(1, H + 1) if upipe.fwd_workspace_bytes(upipe.Shape(S, dm, H, G, d, U, C, sched)) > 0]
+
+
+def _need(upipe, S, dm, H, G, d, U, C, sched):
+    sh = upipe.Shape(S, dm, H, G, d, U, C, sched)
+    return max(upipe.fwd_workspace_bytes(sh), upipe.bwd_workspace_bytes(sh))
+
+
+@pytest.mark.parametrize("S,dm,H,G,d,C,sched", [(32768, 4096, 32, 8, 128, 8, 0), (262144, 4096, 32, 8, 128, 8, 1),
+                                               (131072, 5120, 64, 8, 128, 8, 0), (1024, 512, 8, 2, 64, 2, 0),
+                                               (3072, 1024, 12, 3, 64, 3, 0)])
+def test_choose_u_is_the_largest_width_that_fits(upipe, S, dm, H, G, d, C, sched):
+    """upipe_choose_u against a brute-force scan of the valid widths: the
+    answer fits the budget, the next valid width does not, and it never
+    shrinks as the budget grows."""
+    us = _valid_us(upipe, S, dm, H, G, d, C, sched)
+    assert us and us[-1] <= H
+    needs = {U: _need(upipe, S, dm, H, G, d, U, C, sched) for U in us}
+    budgets = sorted({0, 1} | {n for n in needs.values()} | {n - 1 for n in needs.values()} | {1 << 62})
+    prev = 0
+    for b in budgets:
+        got = upipe.choose_u(S, dm, H, G, d, C, sched, b)
+        want = max([U for U in us if needs[U] <= b], default=0)
+        assert got == want, (b, got, want)
+        assert got >= prev
+        prev = got
+    assert upipe.choose_u(S, dm, H, G, d, C, sched, 1 << 62) == us[-1]
+
+
+def test_choose_u_respects_the_schedule_constraints(upipe):
+    # out of order needs C | G or G | C: with G = 3, C = 2 no width is valid
+    assert upipe.choose_u(1024, 512, 12, 3, 64, 2, 1, 1 << 62) == 0
+    # in order the same shape has valid widths (C | U, U | H)
+    assert upipe.choose_u(1024, 512, 12, 3, 64, 2, 0, 1 << 62) == 12
