@@ -22,7 +22,8 @@ OK, EINVAL, ENOSPC, EUNSUPPORTED, ECUDA, ETIMEOUT = range(6)
 
 # Entry points declared in include/upipe.h
 EXPORTS = (
-    "upipe_fwd_workspace_bytes", "upipe_bwd_workspace_bytes", "upipe_attn_fwd", "upipe_attn_bwd",
+    "upipe_fwd_workspace_bytes", "upipe_fwd_workspace_bytes_prefetch", "upipe_bwd_workspace_bytes",
+    "upipe_attn_fwd", "upipe_attn_bwd",
     "upipe_layout_seq2head", "upipe_layout_head2seq", "upipe_schedule_table", "upipe_choose_u",
     "upipe_attention_fwd", "upipe_attention_bwd", "upipe_attention_bwd_noalloc", "upipe_gemm_bf16",
     "upipe_sync_status", "upipe_status_str", "upipe_version", "upipe_profile_enable", "upipe_profile_read",
@@ -62,6 +63,7 @@ def _sig(lib):
     i32p = ctypes.POINTER(ctypes.c_int32)
     spec = {
         "upipe_fwd_workspace_bytes": (Z, [I] * 8),
+        "upipe_fwd_workspace_bytes_prefetch": (Z, [I] * 8),
         "upipe_bwd_workspace_bytes": (Z, [I] * 8),
         "upipe_attn_fwd": (I, [P, P, P] + [I] * 8 + [P, P, P, P, Z, P, ctypes.POINTER(Stats)]),
         "upipe_attn_bwd": (I, [P, P, P] + [I] * 8 + [P, P, P, P, P, P, P, Z, P, ctypes.POINTER(Stats)]),
@@ -142,6 +144,12 @@ def fwd_workspace_bytes(sh: Shape) -> int:
     return int(lib().upipe_fwd_workspace_bytes(*sh.args()))
 
 
+def fwd_workspace_bytes_prefetch(sh: Shape) -> int:
+    """Forward workspace that lets the next stage's projection and exchange
+    overlap the current stage's attention (see upipe_fwd_workspace_bytes_prefetch)."""
+    return int(lib().upipe_fwd_workspace_bytes_prefetch(*sh.args()))
+
+
 def bwd_workspace_bytes(sh: Shape) -> int:
     return int(lib().upipe_bwd_workspace_bytes(*sh.args()))
 
@@ -167,8 +175,10 @@ def _workspace(nbytes, device):
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
-def attn_fwd(X, W_qkv, W_o, sh: Shape, Y=None, O_saved=None, lse=None, ws=None, stream=None):
-    """Layer forward.  Returns (Y, O_saved, lse, stats)."""
+def attn_fwd(X, W_qkv, W_o, sh: Shape, Y=None, O_saved=None, lse=None, ws=None, stream=None, prefetch=False):
+    """Layer forward.  Returns (Y, O_saved, lse, stats).  prefetch=True sizes the
+    workspace (when none is given) so that the next stage is fetched while the
+    current one computes."""
     torch = _torch()
     bf, f32 = torch.bfloat16, torch.float32
     dev = X.device
@@ -179,6 +189,8 @@ def attn_fwd(X, W_qkv, W_o, sh: Shape, Y=None, O_saved=None, lse=None, ws=None, 
     need = fwd_workspace_bytes(sh)
     if need == 0:
         raise UpipeError("upipe_fwd_workspace_bytes", EINVAL, "invalid shape")
+    if prefetch:
+        need = max(need, fwd_workspace_bytes_prefetch(sh))
     ws = _workspace(need, dev) if ws is None else ws
     st = Stats()
     _check("upipe_attn_fwd", lib().upipe_attn_fwd(

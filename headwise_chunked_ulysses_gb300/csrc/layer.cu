@@ -154,6 +154,8 @@ struct Plan {
   std::vector<int> resident;  // out of order: KV head of each resident slot
   // workspace layout (bytes)
   size_t off_seq = 0, off_qkvh = 0, off_doh = 0, off_dsum = 0, off_lse2 = 0, off_dacc = 0, off_acc32 = 0;
+  bool prefetch = false;            // forward: a second stage-buffer set for the next stage
+  size_t off_seq2 = 0, off_qkvh2 = 0;
   size_t arena = 0, persistent = 0, total = 0;
 };
 
@@ -224,7 +226,7 @@ void build_schedule(Plan& p) {
 // Workspace: [stage arena | persistent].  The stage arena holds the sequence-
 // layout stage buffer (QKV, then reused for dO and dQKV) and the head-layout
 // exchange buffers; the persistent part holds the fp32 Y / dX accumulator.
-Plan make_plan(const Shape& s, bool backward) {
+Plan make_plan(const Shape& s, bool backward, bool prefetch = false) {
   Plan p;
   p.sh = s;
   build_schedule(p);
@@ -243,6 +245,16 @@ Plan make_plan(const Shape& s, bool backward) {
     o = align256(o + U * S * 4);
     p.off_dacc = o;
     o = align256(o + (U + 2 * p.n_kv_slots) * S * d * 4);
+  }
+  if (prefetch && !backward) {
+    // odd stages' buffers: the sequence buffer and the head-layout Q slots,
+    // plus (in order) their own K and V slots; out of order the K and V slots
+    // of the first set stay resident for every stage
+    p.prefetch = true;
+    p.off_seq2 = o;
+    o = align256(o + S * p.max_cols * d * 2);
+    p.off_qkvh2 = o;
+    o = align256(o + (s.sched == UPIPE_SCHED_GQA_OOO ? U : U + 2 * p.n_kv_slots) * S * d * 2);
   }
   p.arena = o;
   const int acc_gemms = backward ? p.n_stages + (s.sched == UPIPE_SCHED_GQA_OOO ? 1 : 0) : p.n_stages;
@@ -285,6 +297,19 @@ std::vector<int> stage_wqkv_heads(const Shape& s, const std::vector<int>& q, con
 
 // Optional per-launch timing: CUDA events recorded on the caller's stream
 // around every kernel, summed per kernel kind by upipe_profile_read().
+// A second stream per device for work that runs beside the caller's stream
+// (created on first use, kept for the life of the process).
+cudaStream_t side_stream() {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+    streams[dev] = nullptr;
+  return streams[dev];
+}
+
 struct Profiler {
   bool on = false;
   std::vector<cudaEvent_t> ev;  // pairs
@@ -323,6 +348,16 @@ struct Launcher {
   double bytes[UPIPE_KERNEL_KINDS] = {};
   cudaError_t err = cudaSuccess;
   bool ok() const { return err == cudaSuccess; }
+  void merge(const Launcher& o) {  // counts and first error of work issued on another stream
+    launches += o.launches;
+    permute_bytes += o.permute_bytes;
+    for (int k = 0; k < UPIPE_KERNEL_KINDS; ++k) {
+      n_kind[k] += o.n_kind[k];
+      flops[k] += o.flops[k];
+      bytes[k] += o.bytes[k];
+    }
+    if (ok() && !o.ok()) err = o.err;
+  }
   template <typename F>
   void run(int kind, double fl, double by, F&& f) {
     if (!ok()) return;
@@ -378,11 +413,11 @@ struct Launcher {
 
 // QKV projection of one stage into the sequence buffer, then the exchange.
 void project_and_exchange(Launcher& L, const Plan& p, int i, const uint16_t* X, const uint16_t* W_qkv,
-                          uint8_t* ws) {
+                          uint8_t* ws, int set = 0) {
   const Shape& s = p.sh;
   const Stage& g = p.st[i];
-  uint16_t* seq = reinterpret_cast<uint16_t*>(ws + p.off_seq);
-  uint16_t* qkvh = reinterpret_cast<uint16_t*>(ws + p.off_qkvh);
+  uint16_t* seq = reinterpret_cast<uint16_t*>(ws + (set ? p.off_seq2 : p.off_seq));
+  uint16_t* qkvh = reinterpret_cast<uint16_t*>(ws + (set ? p.off_qkvh2 : p.off_qkvh));
   const int ncols = g.ncols();
   GemmDesc gd;
   gd.A = X; gd.lda = s.dm; gd.a_rows = s.S; gd.a_cols = s.dm; gd.a_mn = false;
@@ -448,6 +483,12 @@ size_t upipe_fwd_workspace_bytes(int S, int d_model, int H, int G, int d_head, i
   return make_plan(s, false).total;
 }
 
+size_t upipe_fwd_workspace_bytes_prefetch(int S, int d_model, int H, int G, int d_head, int U, int C, int sched) {
+  const Shape s{S, d_model, H, G, d_head, U, C, sched};
+  if (check_shape(s) != UPIPE_OK) return 0;
+  return make_plan(s, false, true).total;
+}
+
 size_t upipe_bwd_workspace_bytes(int S, int d_model, int H, int G, int d_head, int U, int C, int sched) {
   const Shape s{S, d_model, H, G, d_head, U, C, sched};
   if (check_shape(s) != UPIPE_OK) return 0;
@@ -459,26 +500,64 @@ int upipe_attn_fwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
                    void* ws, size_t ws_bytes, void* stream, upipe_stats* stats) {
   const Shape s{S, d_model, H, G, d_head, U, C, sched};
   if (check_shape(s) != UPIPE_OK) return check_shape(s);
-  const Plan p = make_plan(s, false);
+  const Plan pmin = make_plan(s, false);
   const void* ptrs[] = {X, W_qkv, W_o, Y, O_saved, lse};
-  int rc = common_checks(s, ptrs, 6, ws, ws_bytes, p.total);
+  int rc = common_checks(s, ptrs, 6, ws, ws_bytes, pmin.total);
   if (rc != UPIPE_OK) return rc;
-  Launcher L{static_cast<cudaStream_t>(stream), status_ptr()};
+  // with room for a second stage-buffer set, stage i+1's projection and
+  // exchange run on a second stream while stage i's attention runs
+  const Plan ppf = pmin.n_stages > 1 ? make_plan(s, false, true) : pmin;
+  const bool pf = ppf.prefetch && ws_bytes >= ppf.total;
+  const Plan& p = pf ? ppf : pmin;
+  cudaStream_t st0 = static_cast<cudaStream_t>(stream), st1 = nullptr;
+  cudaEvent_t ev[6] = {};  // fork, join, ready[2], free[2]
+  if (pf) {
+    st1 = side_stream();
+    if (!st1) return UPIPE_ECUDA;
+    for (cudaEvent_t& e : ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+        for (cudaEvent_t& f : ev)
+          if (f) cudaEventDestroy(f);
+        return UPIPE_ECUDA;
+      }
+  }
+  cudaEvent_t ev_fork = ev[0], ev_join = ev[1], *ev_ready = ev + 2, *ev_free = ev + 4;
+  Launcher L{st0, status_ptr()};
+  Launcher L2{st1, L.status};
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int d = d_head;
-  uint16_t* qkvh = reinterpret_cast<uint16_t*>(w + p.off_qkvh);
-  uint16_t* oh = reinterpret_cast<uint16_t*>(w + p.off_seq);  // the sequence buffer is dead after the exchange
   float* y32 = reinterpret_cast<float*>(w + p.off_acc32);
   const size_t slot_elems = static_cast<size_t>(S) * d;
-  for (int i = 0; i < p.n_stages && L.ok(); ++i) {
+  if (pf) {  // stage 0's projection and exchange, after the caller's prior work
+    cudaEventRecord(ev_fork, st0);
+    cudaStreamWaitEvent(st1, ev_fork, 0);
+    project_and_exchange(L2, p, 0, X, W_qkv, w, 0);
+    cudaEventRecord(ev_ready[0], st1);
+  }
+  for (int i = 0; i < p.n_stages && L.ok() && L2.ok(); ++i) {
     const Stage& g = p.st[i];
-    // (1) projection, (2) exchange to head shards
-    project_and_exchange(L, p, i, X, W_qkv, w);
+    const int set = pf ? (i & 1) : 0;
+    uint16_t* qkvh = reinterpret_cast<uint16_t*>(w + (set ? p.off_qkvh2 : p.off_qkvh));
+    // K and V: out of order they stay resident in the first set
+    uint16_t* kvh = reinterpret_cast<uint16_t*>(w + (set && sched != UPIPE_SCHED_GQA_OOO ? p.off_qkvh2 : p.off_qkvh));
+    uint16_t* oh = reinterpret_cast<uint16_t*>(w + (set ? p.off_seq2 : p.off_seq));  // dead after the exchange
+    // (1) projection, (2) exchange to head shards: on the second stream, one
+    // stage ahead, into the other buffer set once the stage before has left it
+    if (pf) {
+      if (i + 1 < p.n_stages) {
+        if (i >= 1) cudaStreamWaitEvent(st1, ev_free[(i + 1) & 1], 0);
+        project_and_exchange(L2, p, i + 1, X, W_qkv, w, (i + 1) & 1);
+        cudaEventRecord(ev_ready[(i + 1) & 1], st1);
+      }
+      cudaStreamWaitEvent(st0, ev_ready[set], 0);
+    } else {
+      project_and_exchange(L, p, i, X, W_qkv, w);
+    }
     // (3) attention of the stage's heads
     AttnFwdDesc a;
     a.Q = qkvh;
-    a.K = qkvh + U * slot_elems;
-    a.V = qkvh + (U + p.n_kv_slots) * slot_elems;
+    a.K = kvh + U * slot_elems;
+    a.V = kvh + (U + p.n_kv_slots) * slot_elems;
     a.O = oh;
     a.lse = lse;
     a.S = S; a.D = d; a.n_qslots = U; a.n_kvslots = p.n_kv_slots;
@@ -498,6 +577,7 @@ int upipe_attn_fwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
       b.src_slot[k] = static_cast<uint16_t>(k);
     }
     L.h2s(b);
+    if (pf) cudaEventRecord(ev_free[set], st0);  // this set's buffers are free again
     // (5) the stage's heads' share of the output projection accumulates into Y:
     // fp32 Y32 = O_s W_o[rows of s] for the first stage, += for the next ones
     // (TMA stores / atomic adds), bf16 Y = Y32 + the last share
@@ -517,6 +597,12 @@ int upipe_attn_fwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
       go.out = Y; go.ldo = d_model; go.out_mode = kOutBf16PlusF32; go.aux = y32; go.ld_aux = d_model;
     }
     L.gemm(go);
+  }
+  if (pf) {
+    cudaEventRecord(ev_join, st1);
+    cudaStreamWaitEvent(st0, ev_join, 0);
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    L.merge(L2);
   }
   return finish(L, p, stats);
 }

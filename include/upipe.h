@@ -96,6 +96,18 @@ typedef struct {
 /* Workspace sizes in bytes for the layer calls (0 if the shape is invalid). */
 size_t upipe_fwd_workspace_bytes(int S, int d_model, int H, int G, int d_head, int U, int C, int sched);
 size_t upipe_bwd_workspace_bytes(int S, int d_model, int H, int G, int d_head, int U, int C, int sched);
+/*
+ * Forward workspace with a second stage-buffer set ("Untied Ulysses" summary,
+ * paper.rainbus.top, section on weaknesses from an independent analysis:
+ * fetch the next stage's QKV while the current stage's attention runs).  When
+ * upipe_attn_fwd gets at least this many bytes and the layer has more than
+ * one stage, stage i+1's projection and exchange run on a second stream of
+ * the library while stage i's attention runs on `stream`; results are the
+ * same as with the minimal workspace.  The extra set is O(U): the sequence
+ * buffer and the head-layout Q slots, plus their own K and V slots in the
+ * in-order schedule.  0 if the shape is invalid.
+ */
+size_t upipe_fwd_workspace_bytes_prefetch(int S, int d_model, int H, int G, int d_head, int U, int C, int sched);
 
 /*
  * Forward pass of the layer (Method steps (1)-(4) per stage, plus the
@@ -106,7 +118,13 @@ size_t upipe_bwd_workspace_bytes(int S, int d_model, int H, int G, int d_head, i
  *                   head, kept for the backward pass).
  *   lse           : device, fp32 [H, S], output.
  *   ws            : device workspace of at least upipe_fwd_workspace_bytes() bytes,
- *                   256-byte aligned; contents on entry are ignored.
+ *                   256-byte aligned; contents on entry are ignored.  With at
+ *                   least upipe_fwd_workspace_bytes_prefetch() bytes the next
+ *                   stage is projected and exchanged on a second stream.  The
+ *                   call then orders that stream after `stream`'s prior work
+ *                   and `stream` after all of it, so the caller sees one
+ *                   stream's worth of ordering; calls that overlap on one
+ *                   device share that second stream.
  */
 int upipe_attn_fwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model,
                    int H, int G, int d_head, int U, int C, int sched, upipe_bf16* Y, upipe_bf16* O_saved,

@@ -193,3 +193,21 @@ def test_choose_u_respects_the_schedule_constraints(upipe):
     assert upipe.choose_u(1024, 512, 12, 3, 64, 2, 1, 1 << 62) == 0
     # in order the same shape has valid widths (C | U, U | H)
     assert upipe.choose_u(1024, 512, 12, 3, 64, 2, 0, 1 << 62) == 12
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b_32k", "qwen3_32b_128k"])
+@pytest.mark.parametrize("sched", [0, 1])
+def test_prefetch_workspace_adds_one_stage_set(upipe, name, sched):
+    """The prefetching forward workspace is the minimal one plus a second
+    sequence buffer and head-layout slots: Q slots only out of order (K and V
+    stay resident), Q, K and V in order.  O(U), no H term beyond the plan's."""
+    from synthetic import SHAPES
+    s = SHAPES[name]
+    sh = upipe.Shape(s.S, s.d_model, s.H, s.G, s.d_head, s.U, s.C, sched)
+    base, pf = upipe.fwd_workspace_bytes(sh), upipe.fwd_workspace_bytes_prefetch(sh)
+    assert base > 0 and pf > base
+    slot = s.S * s.d_head * 2
+    head_slots = s.U if sched == 1 else 3 * s.U  # in order every query slot has its own K and V
+    extra = pf - base
+    assert extra >= head_slots * slot
+    assert extra <= head_slots * slot + 3 * s.U * slot + 2 * 256  # + the sequence buffer (<= U + 2 U heads)

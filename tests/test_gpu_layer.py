@@ -60,7 +60,7 @@ def _guard_ok(buf, guard, n):
     return bool((head == 0x5A).all()) and bool((tail == 0x5A).all())
 
 
-def _run(up, ref, U, C, sched, check_guards=False):
+def _run(up, ref, U, C, sched, check_guards=False, prefetch=False):
     import torch
     sh = ref.sh
     s = up.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, U, C, sched)
@@ -73,17 +73,21 @@ def _run(up, ref, U, C, sched, check_guards=False):
                   "dW_o": ((sh.H * sh.d_head, sh.d_model), f32)}
         for k, (shape, dt) in shapes.items():
             outs[k] = _guarded(shape, dt)
+        # the library may use every byte it is given (a larger forward workspace
+        # turns on stage prefetch), so it gets exactly the size, guard after it
         extra = 1 << 20
-        wsf = torch.full((up.fwd_workspace_bytes(s) + extra,), 0xA5, dtype=torch.uint8, device="cuda")
-        wsb = torch.full((up.bwd_workspace_bytes(s) + extra,), 0xA5, dtype=torch.uint8, device="cuda")
+        nf = up.fwd_workspace_bytes_prefetch(s) if prefetch else up.fwd_workspace_bytes(s)
+        nb = up.bwd_workspace_bytes(s)
+        wsf = torch.full((nf + extra,), 0xA5, dtype=torch.uint8, device="cuda")
+        wsb = torch.full((nb + extra,), 0xA5, dtype=torch.uint8, device="cuda")
         Y, O, lse, stf = up.attn_fwd(d["X"], d["W_qkv"], d["W_o"], s, Y=outs["Y"][1], O_saved=outs["O"][1],
-                                     lse=outs["lse"][1], ws=wsf)
+                                     lse=outs["lse"][1], ws=wsf[:nf])
         dX, dWqkv, dWo, stb = up.attn_bwd(d["X"], d["W_qkv"], d["W_o"], O, lse, d["dY"], s, dX=outs["dX"][1],
-                                          dW_qkv=outs["dW_qkv"][1], dW_o=outs["dW_o"][1], ws=wsb)
+                                          dW_qkv=outs["dW_qkv"][1], dW_o=outs["dW_o"][1], ws=wsb[:nb])
         torch.cuda.synchronize()
         for k, (buf, view, guard) in outs.items():
             assert _guard_ok(buf, guard, view.numel()), f"guard band of {k} overwritten"
-        assert bool((wsf[-extra:] == 0xA5).all()) and bool((wsb[-extra:] == 0xA5).all()), "workspace overrun"
+        assert bool((wsf[nf:] == 0xA5).all()) and bool((wsb[nb:] == 0xA5).all()), "workspace overrun"
     else:
         Y, O, lse, stf = up.attn_fwd(d["X"], d["W_qkv"], d["W_o"], s)
         dX, dWqkv, dWo, stb = up.attn_bwd(d["X"], d["W_qkv"], d["W_o"], O, lse, d["dY"], s)
@@ -112,7 +116,7 @@ def _tiny_cases():
 
 @pytest.mark.parametrize("U,C,sched", list(_tiny_cases()))
 def test_tiny_layer_matches_oracle_for_every_u(up, tiny, U, C, sched):
-    out = _run(up, tiny, U, C, sched, check_guards=(U == 2 and C == 2))
+    out = _run(up, tiny, U, C, sched, check_guards=(U == 2 and C == 2), prefetch=(U == 2 and sched == 1))
     e = _errors(tiny, out)
     assert max(e["Y"], e["O"], e["dX"], e["dW_qkv"], e["dW_o"]) <= TOL, e
     # lse is a score-scale quantity: the scores use bf16-rounded projections
@@ -191,3 +195,28 @@ def test_qwen3_32b_128k_sampled_rows(up):
 def test_gqa_schedule_512k_sampled_rows(up):
     """The GQA out-of-order schedule at S=524288 (Llama3-8B widths)."""
     _sampled_rows_check(up, "llama3_8b_512k_gqa", 1, np.array([5, 262143, 524287]))
+
+
+@pytest.mark.parametrize("name,U,C,sched", [("tiny", 2, 2, 0), ("tiny", 2, 2, 1), ("tiny", 4, 2, 1),
+                                            ("llama3_8b_4k", 8, 8, 0), ("llama3_8b_4k", 8, 8, 1)])
+def test_prefetching_forward_is_bit_identical(up, tiny, name, U, C, sched):
+    """With the larger workspace the next stage's projection and exchange run
+    on a second stream during the current stage's attention; the same kernels
+    run on the same data in the same per-stage order, so Y, O and lse are
+    bit-identical to the single-stream forward (and the oracle still holds)."""
+    import torch
+    ref = tiny if name == "tiny" else Ref(SHAPES[name], backward=False)
+    sh = ref.sh
+    s = up.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, U, C, sched)
+    d = ref.dev
+    outs = []
+    for prefetch in (False, True):
+        Y, O, lse, st = up.attn_fwd(d["X"], d["W_qkv"], d["W_o"], s, prefetch=prefetch)
+        torch.cuda.synchronize()
+        up.sync_status()
+        outs.append((Y.view(torch.int16).clone(), O.view(torch.int16).clone(), lse.clone(), st))
+    for a, b in zip(outs[0][:3], outs[1][:3]):
+        assert torch.equal(a, b)
+    assert outs[1][3]["arena_peak_bytes"] > outs[0][3]["arena_peak_bytes"]
+    assert outs[1][3]["launches"] == outs[0][3]["launches"]
+    assert rel(f64_of(outs[1][0].view(torch.bfloat16)), ref.Y) <= TOL
