@@ -27,6 +27,7 @@ EXPORTS = (
     "upipe_layout_seq2head", "upipe_layout_head2seq", "upipe_schedule_table", "upipe_choose_u",
     "upipe_attention_fwd", "upipe_attention_bwd", "upipe_attention_bwd_noalloc", "upipe_gemm_bf16",
     "upipe_sync_status", "upipe_status_str", "upipe_version", "upipe_profile_enable", "upipe_profile_read",
+    "upipe_graphs_enable",
 )
 
 
@@ -79,6 +80,7 @@ def _sig(lib):
         "upipe_status_str": (ctypes.c_char_p, [I]),
         "upipe_version": (I, []),
         "upipe_profile_enable": (I, [I]),
+        "upipe_graphs_enable": (I, [I]),
         "upipe_profile_read": (I, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in spec.items():
@@ -302,6 +304,11 @@ def gemm(A, B, M, N, K, a_trans, b_trans, out_mode=1, D=None, stream=None):
 
 def profile_enable(on=True):
     _check("upipe_profile_enable", lib().upipe_profile_enable(1 if on else 0))
+
+
+def graphs_enable(on=True):
+    """Replay layer calls with unchanged arguments as captured CUDA graphs (off clears the cache)."""
+    _check("upipe_graphs_enable", lib().upipe_graphs_enable(1 if on else 0))
 
 
 def profile_read():

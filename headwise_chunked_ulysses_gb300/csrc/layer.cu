@@ -495,9 +495,13 @@ size_t upipe_bwd_workspace_bytes(int S, int d_model, int H, int G, int d_head, i
   return make_plan(s, true).total;
 }
 
-int upipe_attn_fwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model, int H,
+}  // extern "C"
+
+namespace {
+
+int attn_fwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model, int H,
                    int G, int d_head, int U, int C, int sched, upipe_bf16* Y, upipe_bf16* O_saved, float* lse,
-                   void* ws, size_t ws_bytes, void* stream, upipe_stats* stats) {
+                   void* ws, size_t ws_bytes, void* stream, upipe_stats* stats, bool allow_prefetch) {
   const Shape s{S, d_model, H, G, d_head, U, C, sched};
   if (check_shape(s) != UPIPE_OK) return check_shape(s);
   const Plan pmin = make_plan(s, false);
@@ -507,7 +511,7 @@ int upipe_attn_fwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
   // with room for a second stage-buffer set, stage i+1's projection and
   // exchange run on a second stream while stage i's attention runs
   const Plan ppf = pmin.n_stages > 1 ? make_plan(s, false, true) : pmin;
-  const bool pf = ppf.prefetch && ws_bytes >= ppf.total;
+  const bool pf = allow_prefetch && ppf.prefetch && ws_bytes >= ppf.total;
   const Plan& p = pf ? ppf : pmin;
   cudaStream_t st0 = static_cast<cudaStream_t>(stream), st1 = nullptr;
   cudaEvent_t ev[6] = {};  // fork, join, ready[2], free[2]
@@ -607,7 +611,7 @@ int upipe_attn_fwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
   return finish(L, p, stats);
 }
 
-int upipe_attn_bwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model, int H,
+int attn_bwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model, int H,
                    int G, int d_head, int U, int C, int sched, const upipe_bf16* O_saved, const float* lse,
                    const upipe_bf16* dY, upipe_bf16* dX, float* dW_qkv, float* dW_o, void* ws, size_t ws_bytes,
                    void* stream, upipe_stats* stats) {
@@ -773,6 +777,143 @@ int upipe_attn_bwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
   L.gemm(gwo);
   return finish(L, p, stats);
 }
+
+// ---------------------------------------------------------------------------
+// CUDA-graph replay of whole layer calls (opt-in, upipe_graphs_enable): the
+// launch sequence of a call is captured once on a private stream and replayed
+// on the caller's stream by later calls with the same arguments, removing the
+// per-launch host gaps that dominate short sequences.
+// ---------------------------------------------------------------------------
+struct GraphEntry {
+  std::vector<unsigned long long> key;
+  cudaGraphExec_t exec = nullptr;
+  upipe_stats stats{};
+};
+struct GraphCache {
+  std::mutex mu;
+  bool on = false;
+  std::vector<GraphEntry> entries;  // at most kMaxGraphs; later calls run uncached
+  static constexpr size_t kMaxGraphs = 32;
+};
+GraphCache g_graphs;
+
+cudaStream_t capture_stream() {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+    streams[dev] = nullptr;
+  return streams[dev];
+}
+
+// Runs issue(stream, stats) directly, or through a cached graph of it.
+template <typename F>
+int run_graphed(std::vector<unsigned long long> key, void* stream, upipe_stats* stats, F&& issue) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  bool use = false;
+  {
+    std::lock_guard<std::mutex> g(g_graphs.mu);
+    use = g_graphs.on;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (use && (g_prof.on || cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone))
+    use = false;  // profiling needs per-launch events; a capturing caller captures the launches itself
+  if (!use) return issue(stream, stats);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return UPIPE_ECUDA;
+  key.push_back(static_cast<unsigned long long>(dev));
+  {
+    std::lock_guard<std::mutex> g(g_graphs.mu);
+    for (const GraphEntry& e : g_graphs.entries)
+      if (e.key == key) {
+        if (stats) *stats = e.stats;
+        return cudaGraphLaunch(e.exec, st) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
+      }
+    if (g_graphs.entries.size() >= GraphCache::kMaxGraphs) return issue(stream, stats);
+  }
+  cudaStream_t cap = capture_stream();
+  if (!cap || !status_ptr()) return UPIPE_ECUDA;  // lazily created state exists before capture begins
+  // Nothing issued on the capture stream executes; the graph launch below
+  // orders the work after the caller's prior work on its own stream.
+  if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed) != cudaSuccess) return UPIPE_ECUDA;
+  upipe_stats local{};
+  const int rc = issue(static_cast<void*>(cap), &local);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(cap, &graph);
+  if (rc != UPIPE_OK || ec != cudaSuccess || !graph) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc != UPIPE_OK ? rc : UPIPE_ECUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ei != cudaSuccess) return UPIPE_ECUDA;
+  {
+    std::lock_guard<std::mutex> g(g_graphs.mu);
+    GraphEntry e;
+    e.key = std::move(key);
+    e.exec = exec;
+    e.stats = local;
+    g_graphs.entries.push_back(std::move(e));
+  }
+  if (stats) *stats = local;
+  return cudaGraphLaunch(exec, st) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
+}
+
+unsigned long long as_key(const void* p) { return static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(p)); }
+
+}  // namespace
+
+extern "C" {
+
+int upipe_attn_fwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model, int H,
+                   int G, int d_head, int U, int C, int sched, upipe_bf16* Y, upipe_bf16* O_saved, float* lse,
+                   void* ws, size_t ws_bytes, void* stream, upipe_stats* stats) {
+  std::vector<unsigned long long> key = {1ull, as_key(X), as_key(W_qkv), as_key(W_o), as_key(Y), as_key(O_saved),
+                                         as_key(lse), as_key(ws), ws_bytes};
+  for (int v : {S, d_model, H, G, d_head, U, C, sched}) key.push_back(static_cast<unsigned long long>(v));
+  // a graph is replayed on one stream: the prefetching path is used only uncached
+  bool graphs_on;
+  {
+    std::lock_guard<std::mutex> g(g_graphs.mu);
+    graphs_on = g_graphs.on;
+  }
+  return run_graphed(std::move(key), stream, stats, [&](void* st, upipe_stats* sts) {
+    return attn_fwd_issue(X, W_qkv, W_o, S, d_model, H, G, d_head, U, C, sched, Y, O_saved, lse, ws, ws_bytes, st,
+                          sts, !graphs_on);
+  });
+}
+
+int upipe_attn_bwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model, int H,
+                   int G, int d_head, int U, int C, int sched, const upipe_bf16* O_saved, const float* lse,
+                   const upipe_bf16* dY, upipe_bf16* dX, float* dW_qkv, float* dW_o, void* ws, size_t ws_bytes,
+                   void* stream, upipe_stats* stats) {
+  std::vector<unsigned long long> key = {2ull, as_key(X), as_key(W_qkv), as_key(W_o), as_key(O_saved), as_key(lse),
+                                         as_key(dY), as_key(dX), as_key(dW_qkv), as_key(dW_o), as_key(ws), ws_bytes};
+  for (int v : {S, d_model, H, G, d_head, U, C, sched}) key.push_back(static_cast<unsigned long long>(v));
+  return run_graphed(std::move(key), stream, stats, [&](void* st, upipe_stats* sts) {
+    return attn_bwd_issue(X, W_qkv, W_o, S, d_model, H, G, d_head, U, C, sched, O_saved, lse, dY, dX, dW_qkv, dW_o, ws,
+                          ws_bytes, st, sts);
+  });
+}
+
+int upipe_graphs_enable(int on) {
+  std::vector<GraphEntry> old;
+  {
+    std::lock_guard<std::mutex> g(g_graphs.mu);
+    g_graphs.on = on != 0;
+    if (!g_graphs.on) old.swap(g_graphs.entries);
+  }
+  if (!old.empty()) {
+    // replays may still be in flight on any stream
+    if (cudaDeviceSynchronize() != cudaSuccess) return UPIPE_ECUDA;
+    for (GraphEntry& e : old) cudaGraphExecDestroy(e.exec);
+  }
+  return UPIPE_OK;
+}
+
 
 int upipe_layout_seq2head(const upipe_bf16* src, upipe_bf16* dst, int S, int n_heads, int d_head, int C,
                           int src_row_stride, void* stream) {

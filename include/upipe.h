@@ -259,6 +259,28 @@ int upipe_version(void);
 int upipe_profile_enable(int on);
 int upipe_profile_read(double* ms_by_kind, int* count_by_kind);
 
+/*
+ * Optional CUDA-graph replay of whole layer calls, off by default (the
+ * short-sequence overhead named in the "Untied Ulysses" summary page's
+ * weaknesses section: a layer call issues several dozen small launches, whose
+ * host-side gaps are a visible share of a short step).  When enabled, the first
+ * upipe_attn_fwd / upipe_attn_bwd call with a given argument list (every
+ * pointer, size and the device) captures its launch sequence on a private
+ * stream into a graph and launches that graph on the caller's stream; later
+ * calls with the same argument list replay it.  Replays read the CURRENT
+ * contents of the same buffers, so the caller keeps the buffers alive and
+ * unmoved while graphs are on; calls with other pointers capture a new graph
+ * (up to 32 are kept; further argument lists run uncached).  Results are
+ * bit-identical to direct calls.  Calls run directly, without a graph, while
+ * upipe_profile_enable is on, when the caller's stream is itself being
+ * captured, and the forward never uses its prefetching schedule under a graph
+ * (a prefetch-sized workspace is accepted and runs the single-stream plan).
+ * The stats a replay reports are those of the captured call.
+ * upipe_graphs_enable(0) waits for the device and destroys every cached graph.
+ * Errors: UPIPE_ECUDA when capture, instantiation or launch fails.
+ */
+int upipe_graphs_enable(int on);
+
 #ifdef __cplusplus
 }
 #endif
