@@ -484,6 +484,134 @@ def _kv_back_and_project(dK_held, dV_held, heads_of, Xs, Wk, Wv, dX, dW_qkv, H, 
 
 
 # ---------------------------------------------------------------------------
+# head stages combined with sequence chunks ([U1] Limitations and Future
+# directions: FPDT chunks the sequence, UPipe the heads; the two are
+# orthogonal and the pages suggest combining them)
+# ---------------------------------------------------------------------------
+
+def chunk_scores(q, k, q_pos, k_pos):
+    """Scores of a query chunk whose first row sits at sequence position q_pos
+    against a key chunk starting at k_pos: q k^T / sqrt(d), -inf where the
+    key's position is after the query's."""
+    A = (q @ k.T) / np.sqrt(q.shape[1])
+    qi = q_pos + np.arange(q.shape[0])[:, None]
+    kj = k_pos + np.arange(k.shape[0])[None, :]
+    A[kj > qi] = -np.inf
+    return A
+
+
+def partial_attention(q, k, v, q_pos, k_pos):
+    """Attention of a query chunk over one key chunk: the normalised partial
+    output and its log-sum-exp (every row sees at least one key)."""
+    A = chunk_scores(q, k, q_pos, k_pos)
+    m = A.max(axis=1, keepdims=True)
+    E = np.exp(A - m)
+    l = E.sum(axis=1, keepdims=True)
+    return (E / l) @ v, (m + np.log(l))[:, 0]
+
+
+def merge_partials(o_a, lse_a, o_b, lse_b):
+    """Softmax over the union of two disjoint key sets from the two partial
+    results: weights exp(lse_x - lse) with lse = log(exp(lse_a) + exp(lse_b))."""
+    lse = np.logaddexp(lse_a, lse_b)
+    return o_a * np.exp(lse_a - lse)[:, None] + o_b * np.exp(lse_b - lse)[:, None], lse
+
+
+def _check_chunks(S, C, n_chunks):
+    if n_chunks <= 0 or S % n_chunks or (S // n_chunks) % C:
+        raise ValueError("n_chunks must divide S into chunks the C ranks split evenly")
+
+
+def chunked_forward(X, W_qkv, W_o, H, G, d_head, U, C, n_chunks):
+    """The in-order head stages run on sequence chunks of S/n_chunks tokens.
+
+    For chunk i (ascending) and stage s: project the chunk's rows onto the
+    stage's Q heads and the KV heads they use; the chunk's K and V go to an
+    offload store; each query head attends to KV chunks 0..i of the store, the
+    partial results merged by log-sum-exp; the stage's share of the output
+    projection is added to the chunk's rows of Y.  Returns (Y, O, lse) like
+    ``layer_forward``.
+    """
+    S, d_model = X.shape
+    check_shape(S, d_model, H, G, d_head, U, C, IN_ORDER)
+    _check_chunks(S, C, n_chunks)
+    d, Sc = d_head, S // n_chunks
+    Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
+    sched = stage_heads(H, G, U, C, IN_ORDER)
+    store_K, store_V = {}, {}
+    Y = np.zeros((S, d_model))
+    O = np.zeros((S, H * d))
+    lse = np.zeros((H, S))
+    for i in range(n_chunks):
+        rows = slice(i * Sc, (i + 1) * Sc)
+        Xi = X[rows]
+        for st in range(H // U):
+            heads = [int(h) for h in sched[st].reshape(-1)]
+            for g in sorted({kv_head(h, H, G) for h in heads}):
+                store_K[g, i] = Xi @ Wk[g]
+                store_V[g, i] = Xi @ Wv[g]
+            for h in heads:
+                g = kv_head(h, H, G)
+                q = Xi @ Wq[h]
+                o, l = partial_attention(q, store_K[g, 0], store_V[g, 0], i * Sc, 0)
+                for j in range(1, i + 1):
+                    o_j, l_j = partial_attention(q, store_K[g, j], store_V[g, j], i * Sc, j * Sc)
+                    o, l = merge_partials(o, l, o_j, l_j)
+                O[rows, h * d:(h + 1) * d] = o
+                lse[h, rows] = l
+                Y[rows] += o @ W_o[h * d:(h + 1) * d, :]
+    return Y, O, lse
+
+
+def chunked_backward(X, W_qkv, W_o, H, G, d_head, U, C, n_chunks, dY, O_saved, lse):
+    """Backward of ``chunked_forward``: query chunks in descending order.
+
+    The K and V chunks are recomputed into the store first.  For query chunk i
+    and stage s, each head's P against KV chunk j <= i is rebuilt from the
+    saved log-sum-exp; dQ of the chunk sums over j, dK and dV of chunk j sum
+    over the query chunks i >= j (and the query heads of the KV head).  Chunk
+    i's dK, dV are complete once query chunk i is done (later chunks came
+    first), and go into dX and dW_qkv then.  Returns (dX, dW_qkv, dW_o).
+    """
+    S, d_model = X.shape
+    check_shape(S, d_model, H, G, d_head, U, C, IN_ORDER)
+    _check_chunks(S, C, n_chunks)
+    d, Sc = d_head, S // n_chunks
+    Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
+    sched = stage_heads(H, G, U, C, IN_ORDER)
+    store_K = {(g, j): X[j * Sc:(j + 1) * Sc] @ Wk[g] for g in range(G) for j in range(n_chunks)}
+    store_V = {(g, j): X[j * Sc:(j + 1) * Sc] @ Wv[g] for g in range(G) for j in range(n_chunks)}
+    dK = {key: np.zeros((Sc, d)) for key in store_K}
+    dV = {key: np.zeros((Sc, d)) for key in store_V}
+    dX = np.zeros_like(X)
+    dW_qkv = np.zeros_like(W_qkv)
+    for i in reversed(range(n_chunks)):
+        rows = slice(i * Sc, (i + 1) * Sc)
+        Xi = X[rows]
+        for st in range(H // U):
+            for h in [int(h) for h in sched[st].reshape(-1)]:
+                g = kv_head(h, H, G)
+                q = Xi @ Wq[h]
+                do = dY[rows] @ W_o[h * d:(h + 1) * d, :].T
+                Dsum = (do * O_saved[rows, h * d:(h + 1) * d]).sum(axis=1, keepdims=True)
+                dq = np.zeros((Sc, d))
+                for j in range(i + 1):
+                    k, v = store_K[g, j], store_V[g, j]
+                    P = np.exp(chunk_scores(q, k, i * Sc, j * Sc) - lse[h, rows][:, None])
+                    dV[g, j] += P.T @ do
+                    dA = P * (do @ v.T - Dsum)
+                    dq += dA @ k / np.sqrt(d)
+                    dK[g, j] += dA.T @ q / np.sqrt(d)
+                dX[rows] += dq @ Wq[h].T
+                dW_qkv[:, h * d:(h + 1) * d] += Xi.T @ dq
+        for g in range(G):
+            dX[rows] += dK[g, i] @ Wk[g].T + dV[g, i] @ Wv[g].T
+            dW_qkv[:, (H + g) * d:(H + g + 1) * d] += Xi.T @ dK[g, i]
+            dW_qkv[:, (H + G + g) * d:(H + G + g + 1) * d] += Xi.T @ dV[g, i]
+    return dX, dW_qkv, O_saved.T @ dY
+
+
+# ---------------------------------------------------------------------------
 # FLOP accounting (model FLOPs; not a method step)
 # ---------------------------------------------------------------------------
 
