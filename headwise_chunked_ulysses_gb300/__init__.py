@@ -27,7 +27,8 @@ EXPORTS = (
     "upipe_layout_seq2head", "upipe_layout_head2seq", "upipe_schedule_table", "upipe_choose_u",
     "upipe_attention_fwd", "upipe_attention_bwd", "upipe_attention_bwd_noalloc", "upipe_gemm_bf16",
     "upipe_sync_status", "upipe_status_str", "upipe_version", "upipe_profile_enable", "upipe_profile_read",
-    "upipe_graphs_enable",
+    "upipe_graphs_enable", "upipe_chunked_workspace_bytes", "upipe_chunked_store_bytes",
+    "upipe_attn_fwd_chunked", "upipe_attn_bwd_chunked",
 )
 
 
@@ -46,7 +47,8 @@ class Stats(ctypes.Structure):
                 ("launches", ctypes.c_int), ("stages", ctypes.c_int),
                 ("launches_by_kind", ctypes.c_int * len(KERNEL_KINDS)),
                 ("flops_by_kind", ctypes.c_double * len(KERNEL_KINDS)),
-                ("bytes_by_kind", ctypes.c_double * len(KERNEL_KINDS))]
+                ("bytes_by_kind", ctypes.c_double * len(KERNEL_KINDS)),
+                ("offload_bytes", ctypes.c_size_t), ("offload_copy_bytes", ctypes.c_size_t)]
 
     def as_dict(self):
         d = {}
@@ -81,6 +83,10 @@ def _sig(lib):
         "upipe_version": (I, []),
         "upipe_profile_enable": (I, [I]),
         "upipe_graphs_enable": (I, [I]),
+        "upipe_chunked_workspace_bytes": (Z, [I] * 9),
+        "upipe_chunked_store_bytes": (Z, [I] * 9),
+        "upipe_attn_fwd_chunked": (I, [P, P, P] + [I] * 8 + [P, P, P, P, Z, P, Z, P, P]),
+        "upipe_attn_bwd_chunked": (I, [P, P, P] + [I] * 8 + [P, P, P, P, P, P, P, Z, P, Z, P, P]),
         "upipe_profile_read": (I, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in spec.items():
@@ -222,6 +228,74 @@ def attn_bwd(X, W_qkv, W_o, O_saved, lse, dY, sh: Shape, dX=None, dW_qkv=None, d
         _ptr(O_saved, bf, "O_saved"), _ptr(lse, f32, "lse"), _ptr(dY, bf, "dY"),
         _ptr(dX, bf, "dX"), _ptr(dW_qkv, f32, "dW_qkv"), _ptr(dW_o, f32, "dW_o"),
         _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(st)))
+    return dX, dW_qkv, dW_o, st.as_dict()
+
+
+def chunked_workspace_bytes(sh: Shape, n_chunks, backward) -> int:
+    return int(lib().upipe_chunked_workspace_bytes(*sh.args()[:7], n_chunks, 1 if backward else 0))
+
+
+def chunked_store_bytes(sh: Shape, n_chunks, backward) -> int:
+    return int(lib().upipe_chunked_store_bytes(*sh.args()[:7], n_chunks, 1 if backward else 0))
+
+
+def _store_ptr(store):
+    """The offload store: a CUDA tensor, or a page-locked CPU tensor."""
+    if store.is_cuda:
+        return _ptr(store, None, "store")
+    if not store.is_pinned():
+        raise ValueError("a host store must be page-locked (pin_memory)")
+    if not store.is_contiguous():
+        raise ValueError("store must be contiguous")
+    return ctypes.c_void_p(store.data_ptr())
+
+
+def attn_fwd_chunked(X, W_qkv, W_o, sh: Shape, n_chunks, store, Y=None, O_saved=None, lse=None, ws=None,
+                     stream=None):
+    """Layer forward on sequence chunks (in-order stages); store is the K/V
+    offload store (device or pinned host tensor of chunked_store_bytes()).
+    Returns (Y, O_saved, lse, stats)."""
+    torch = _torch()
+    bf, f32 = torch.bfloat16, torch.float32
+    dev = X.device
+    S, dm, H, d = sh.S, sh.d_model, sh.H, sh.d_head
+    Y = torch.empty(S, dm, dtype=bf, device=dev) if Y is None else Y
+    O_saved = torch.empty(S, H * d, dtype=bf, device=dev) if O_saved is None else O_saved
+    lse = torch.empty(H, S, dtype=f32, device=dev) if lse is None else lse
+    need = chunked_workspace_bytes(sh, n_chunks, False)
+    if need == 0:
+        raise UpipeError("upipe_chunked_workspace_bytes", EINVAL, "invalid shape or chunk count")
+    ws = _workspace(need, dev) if ws is None else ws
+    st = Stats()
+    _check("upipe_attn_fwd_chunked", lib().upipe_attn_fwd_chunked(
+        _ptr(X, bf, "X"), _ptr(W_qkv, bf, "W_qkv"), _ptr(W_o, bf, "W_o"), *sh.args()[:7], n_chunks,
+        _ptr(Y, bf, "Y"), _ptr(O_saved, bf, "O_saved"), _ptr(lse, f32, "lse"),
+        _ptr(ws), ws.numel(), _store_ptr(store), store.numel() * store.element_size(), _stream(stream),
+        ctypes.byref(st)))
+    return Y, O_saved, lse, st.as_dict()
+
+
+def attn_bwd_chunked(X, W_qkv, W_o, O_saved, lse, dY, sh: Shape, n_chunks, store, dX=None, dW_qkv=None,
+                     dW_o=None, ws=None, stream=None):
+    """Layer backward on sequence chunks.  Returns (dX, dW_qkv, dW_o, stats)."""
+    torch = _torch()
+    bf, f32 = torch.bfloat16, torch.float32
+    dev = X.device
+    S, dm, H, G, d = sh.S, sh.d_model, sh.H, sh.G, sh.d_head
+    dX = torch.empty(S, dm, dtype=bf, device=dev) if dX is None else dX
+    dW_qkv = torch.empty(dm, (H + 2 * G) * d, dtype=f32, device=dev) if dW_qkv is None else dW_qkv
+    dW_o = torch.empty(H * d, dm, dtype=f32, device=dev) if dW_o is None else dW_o
+    need = chunked_workspace_bytes(sh, n_chunks, True)
+    if need == 0:
+        raise UpipeError("upipe_chunked_workspace_bytes", EINVAL, "invalid shape or chunk count")
+    ws = _workspace(need, dev) if ws is None else ws
+    st = Stats()
+    _check("upipe_attn_bwd_chunked", lib().upipe_attn_bwd_chunked(
+        _ptr(X, bf, "X"), _ptr(W_qkv, bf, "W_qkv"), _ptr(W_o, bf, "W_o"), *sh.args()[:7], n_chunks,
+        _ptr(O_saved, bf, "O_saved"), _ptr(lse, f32, "lse"), _ptr(dY, bf, "dY"),
+        _ptr(dX, bf, "dX"), _ptr(dW_qkv, f32, "dW_qkv"), _ptr(dW_o, f32, "dW_o"),
+        _ptr(ws), ws.numel(), _store_ptr(store), store.numel() * store.element_size(), _stream(stream),
+        ctypes.byref(st)))
     return dX, dW_qkv, dW_o, st.as_dict()
 
 

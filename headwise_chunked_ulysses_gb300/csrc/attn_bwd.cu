@@ -40,6 +40,7 @@ constexpr int CH = 128 * 128;  // a 64-column chunk of a 128-row bf16 tile
 
 struct BwdArgs {
   int S, n_qslots, n_kvslots, q_blocks;
+  int kv_ld, kv_blocks, q_off_blocks;  // key positions: see AttnBwdDesc
   float scale_log2, scale;
   int accumulate_kv;
   int dq_tiled;
@@ -72,13 +73,15 @@ struct BwdCfg {
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
 };
 
-// The (query slot, query block) pairs a CTA visits, in order.
+// The (query slot, query block) pairs a CTA visits, in order: the query
+// blocks at or after its KV block (query block b sits at KV block
+// b + q_off_blocks).
 struct ItemCursor {
-  int qs = -1, qb = 0, kvb = 0, q_blocks = 0;
+  int qs = -1, qb = 0, qb_first = 0, q_blocks = 0;
   __device__ bool next(const BwdArgs& a, int kvs) {
     if (qs >= 0 && ++qb < q_blocks) return true;
     for (++qs; qs < a.n_qslots; ++qs)
-      if (a.kv_slot[qs] == kvs) { qb = kvb; return true; }
+      if (a.kv_slot[qs] == kvs) { qb = qb_first; return true; }
     return false;
   }
 };
@@ -115,13 +118,14 @@ __global__ void __launch_bounds__(512, 1)
   // (most work) first, so the CTAs running at one time share few slots'
   // query-side data
   const int grp_slots = a.grp_slots;
-  const int per_grp = grp_slots * a.q_blocks;
+  const int per_grp = grp_slots * a.kv_blocks;
   const int grp = static_cast<int>(blockIdx.x) / per_grp, rem = static_cast<int>(blockIdx.x) % per_grp;
   const int kvb = rem / grp_slots;
   const int kvs = grp * grp_slots + rem % grp_slots;
   int n_q = 0;
   for (int i = 0; i < a.n_qslots; ++i) n_q += (a.kv_slot[i] == kvs);
-  const int n_items = n_q * (a.q_blocks - kvb);
+  const int qb_first = max(0, kvb - a.q_off_blocks);
+  const int n_items = n_q * max(0, a.q_blocks - qb_first);
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmdO);
-      const int kv_row = kvs * a.S + kvb * BKV;
+      const int kv_row = kvs * a.kv_ld + kvb * BKV;
       mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
@@ -164,7 +168,7 @@ __global__ void __launch_bounds__(512, 1)
         tma_load_2d(smem + C::V_OFF + c * CH, &tmV, kv_full, c * 64, kv_row);
       }
       ItemCursor cur;
-      cur.kvb = kvb;
+      cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
       for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
         const int st = i & 1;
@@ -265,13 +269,13 @@ __global__ void __launch_bounds__(512, 1)
       const float sl2 = a.scale_log2;
       const uint64_t sl2x2 = f2(sl2, sl2);
       ItemCursor cur;
-      cur.kvb = kvb;
+      cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
       bool ok = true;
       int i = 0;
       for (; i < n_items && cur.next(a, kvs); ++i) {
         const int st = i & 1;
-        const bool diag = (cur.qb == kvb);
+        const bool diag = (cur.qb + a.q_off_blocks == kvb);
         if (!mbar_wait_warp(s_full, i & 1, w, 47)) { ok = false; break; }
         if (!mbar_wait_warp(&qdo_full[st], (i >> 1) & 1, w, 48)) { ok = false; break; }
         tc_fence_after();
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(512, 1)
       // dK, dV epilogue: this thread's half of the d columns of KV row `row`
       if (ok && mbar_wait_warp(kv_done, 0, w, 52)) {
         tc_fence_after();
-        const long long base = (static_cast<long long>(kvs) * a.S + kv_idx) * D + half * (D / 2);
+        const long long base = (static_cast<long long>(kvs) * a.kv_ld + kv_idx) * D + half * (D / 2);
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
           float* dst = (which == 0 ? a.dV : a.dK) + base;
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(512, 1)
       const int row = (warp & 3) * 32 + lane;
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
       ItemCursor cur;
-      cur.kvb = kvb;
+      cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
       for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
         if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
@@ -402,7 +406,7 @@ __global__ void __launch_bounds__(512, 1)
     // a KV slot no query head uses in this launch: its gradient is zero
     const int row = (warp & 3) * 32 + lane;
     const int half = (warp - 4) >> 2;
-    const long long base = (static_cast<long long>(kvs) * a.S + kvb * BKV + row) * D + half * (D / 2);
+    const long long base = (static_cast<long long>(kvs) * a.kv_ld + kvb * BKV + row) * D + half * (D / 2);
     for (int c = 0; c < D / 2; c += 4) {
       *reinterpret_cast<float4*>(a.dK + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
       *reinterpret_cast<float4*>(a.dV + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -445,7 +449,7 @@ __global__ void bwd_prep_kernel(const BwdPrepDesc p) {
   for (int off = lanes_per_row / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (r < total && v == 0) {
     p.Dsum[r] = acc;
-    p.lse2[r] = p.lse[static_cast<long long>(p.lse_row[slot]) * p.S + t] * -1.4426950408889634f;
+    p.lse2[r] = p.lse[static_cast<long long>(p.lse_row[slot]) * (p.lse_ld ? p.lse_ld : p.S) + t] * -1.4426950408889634f;
   }
 }
 
@@ -484,7 +488,7 @@ cudaError_t run_bwd(const CUtensorMap* tm, const BwdArgs& args, cudaStream_t st)
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<args.n_kvslots * args.q_blocks, 512, BwdCfg<D>::SMEM, st>>>(tm[0], tm[1], tm[2], tm[3], args);
+  kern<<<args.n_kvslots * args.kv_blocks, 512, BwdCfg<D>::SMEM, st>>>(tm[0], tm[1], tm[2], tm[3], args);
   return cudaGetLastError();
 }
 
@@ -507,16 +511,24 @@ cudaError_t launch_dq_tiled_to_seq(const DqTiledDesc& p, cudaStream_t st) {
 }
 
 cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) {
+  const int kv_len = d.kv_len ? d.kv_len : d.S;
+  const int kv_ld = d.kv_ld ? d.kv_ld : kv_len;
   if ((d.D != 64 && d.D != 128) || d.S % 128 || d.n_qslots <= 0 || d.n_qslots > kMaxSlots ||
       d.n_kvslots <= 0)
     return cudaErrorInvalidValue;
+  if (kv_len <= 0 || kv_len % 128 || kv_ld < kv_len || d.q_off < 0 || d.q_off % 128) return cudaErrorInvalidValue;
+  for (int i = 0; i < d.n_qslots; ++i)
+    if (d.kv_slot[i] >= d.n_kvslots) return cudaErrorInvalidValue;
   CUtensorMap tm[4];
   if (!make_tmap_bf16(&tm[0], d.Q, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tm[1], d.K, d.D, (uint64_t)d.n_kvslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tm[2], d.V, d.D, (uint64_t)d.n_kvslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tm[1], d.K, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tm[2], d.V, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tm[3], d.dO, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
   BwdArgs a;
   a.S = d.S;
+  a.kv_ld = kv_ld;
+  a.kv_blocks = kv_len / BKV;
+  a.q_off_blocks = d.q_off / BQ;
   a.n_qslots = d.n_qslots;
   a.n_kvslots = d.n_kvslots;
   a.q_blocks = d.S / BQ;

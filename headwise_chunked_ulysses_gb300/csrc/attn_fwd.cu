@@ -37,11 +37,14 @@ constexpr float kRescaleLog2 = 8.0f;
 
 struct FwdArgs {
   int S, n_qslots, q_blocks, q_pairs;
+  int kv_ld, kv_blocks, q_off_blocks, lse_ld, mode;
   float scale_log2;
   uint16_t kv_slot[kMaxSlots];
   uint16_t lse_row[kMaxSlots];
   uint16_t* O;
   float* lse;
+  float* o_acc;
+  float* lse_acc;
   int* status;
 };
 
@@ -93,7 +96,10 @@ __global__ void __launch_bounds__(384, 1)
   const int kvs = a.kv_slot[slot];
   const int qb0 = 2 * t, qb1 = 2 * t + 1;
   const bool has_b = qb1 < a.q_blocks;
-  const int n_kv0 = qb0 + 1, n_kv1 = has_b ? qb1 + 1 : 0;
+  // query block b sits at KV block b + q_off_blocks: it sees the KV blocks up
+  // to that one (the diagonal, masked) or all of them when it lies beyond
+  const int n_kv0 = min(a.kv_blocks, qb0 + a.q_off_blocks + 1);
+  const int n_kv1 = has_b ? min(a.kv_blocks, qb1 + a.q_off_blocks + 1) : 0;
   const int n_blocks = has_b ? n_kv1 : n_kv0;
 
   if (threadIdx.x == 0) {
@@ -141,7 +147,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&k_full[s], C::TILE);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(smem + C::K_OFF + s * C::TILE + c * CH, &tmK, &k_full[s], c * 64, kvs * a.S + j * BKV);
+            tma_load_2d(smem + C::K_OFF + s * C::TILE + c * CH, &tmK, &k_full[s], c * 64, kvs * a.kv_ld + j * BKV);
         }
         if (j > 0) {
           const int jv = j - 1, s = jv & 1;
@@ -149,7 +155,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&v_full[s], C::TILE);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(smem + C::V_OFF + s * C::TILE + c * CH, &tmV, &v_full[s], c * 64, kvs * a.S + jv * BKV);
+            tma_load_2d(smem + C::V_OFF + s * C::TILE + c * CH, &tmV, &v_full[s], c * 64, kvs * a.kv_ld + jv * BKV);
         }
       }
     } else if (warp == 1 && lane == 0) {
@@ -212,7 +218,10 @@ __global__ void __launch_bounds__(384, 1)
       if (tile == 0 || has_b) {
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;
-        const int qi = (tile ? qb1 : qb0) * BQ + row;
+        const int qb = tile ? qb1 : qb0;
+        const int qi = qb * BQ + row;                     // row of the query slot
+        const int qk = qi + a.q_off_blocks * BQ;          // its position among the keys
+        const bool has_diag = qb + a.q_off_blocks < a.kv_blocks;
         const int nkv = tile ? n_kv1 : n_kv0;
         const uint32_t t_s = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + C::t_s(tile);
         const uint32_t t_o = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + C::t_o(tile);
@@ -222,8 +231,8 @@ __global__ void __launch_bounds__(384, 1)
         for (int j = 0; j < nkv; ++j) {
           if (!mbar_wait_warp(&s_full[tile], j & 1, w, 25)) { ok = false; break; }
           tc_fence_after();
-          const bool diag = (j == nkv - 1);
-          const int lim = diag ? qi - j * BKV : BKV;  // keys at column > lim are in the future
+          const bool diag = has_diag && (j == nkv - 1);
+          const int lim = diag ? qk - j * BKV : BKV;  // keys at column > lim are in the future
           // the whole row of S in one TMEM load: its maximum, then P from registers
           uint32_t v[BKV];
           tmem_ld128(t_s, v);
@@ -297,22 +306,73 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (ok && mbar_wait_warp(&o_done[tile], 0, w, 27)) {
           tc_fence_after();
-          const float inv = 1.f / l_run;
-          uint16_t* orow = a.O + (static_cast<long long>(slot) * a.S + qi) * D;
+          const long long orow_idx = static_cast<long long>(slot) * a.S + qi;
+          uint16_t* orow = a.O + orow_idx * D;
+          const float lse2_part = m_run + __log2f(l_run);  // this launch's keys, log2 units
+          float* lrow = a.lse + static_cast<long long>(a.lse_row[slot]) * a.lse_ld + qi;
+          if (a.mode == kFwdPlain) {
+            const float inv = 1.f / l_run;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(t_o + c * 32, v);
-            uint4* o = reinterpret_cast<uint4*>(orow + c * 32);
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld32(t_o + c * 32, v);
+              uint4* o = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              o[i] = make_uint4(pack_bf16(__uint_as_float(v[8 * i]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
-                                pack_bf16(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv),
-                                pack_bf16(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv),
-                                pack_bf16(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
+              for (int i = 0; i < 4; ++i) {
+                o[i] = make_uint4(pack_bf16(__uint_as_float(v[8 * i]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
+                                  pack_bf16(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv),
+                                  pack_bf16(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv),
+                                  pack_bf16(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
+              }
             }
+            *lrow = lse2_part * 0.69314718055994531f;
+          } else {
+            // merge with the running result of the earlier key chunks (fp32
+            // output normalised over its keys, log-sum-exp in log2 units):
+            // weights 2^(lse_x - lse_union)
+            float* acc = a.o_acc + orow_idx * D;
+            float* lacc = a.lse_acc + orow_idx;
+            float wa = 0.f, wb = 1.f / l_run, lse2_new = lse2_part;
+            if (a.mode != kFwdFirst) {
+              const float prev = *lacc;
+              const float m = fmaxf(prev, lse2_part);
+              const float ea = ex2(prev - m), eb = ex2(lse2_part - m);
+              const float inv_s = 1.f / (ea + eb);
+              wa = ea * inv_s;
+              wb = eb * inv_s / l_run;
+              lse2_new = m + __log2f(ea + eb);
+            }
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld32(t_o + c * 32, v);
+              float4* ac = reinterpret_cast<float4*>(acc + c * 32);
+              float x[32];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (a.mode != kFwdFirst) p = ac[i];
+                x[4 * i] = fmaf(__uint_as_float(v[4 * i]), wb, p.x * wa);
+                x[4 * i + 1] = fmaf(__uint_as_float(v[4 * i + 1]), wb, p.y * wa);
+                x[4 * i + 2] = fmaf(__uint_as_float(v[4 * i + 2]), wb, p.z * wa);
+                x[4 * i + 3] = fmaf(__uint_as_float(v[4 * i + 3]), wb, p.w * wa);
+              }
+              if (a.mode == kFwdLast) {
+                uint4* o = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  o[i] = make_uint4(pack_bf16(x[8 * i], x[8 * i + 1]), pack_bf16(x[8 * i + 2], x[8 * i + 3]),
+                                    pack_bf16(x[8 * i + 4], x[8 * i + 5]), pack_bf16(x[8 * i + 6], x[8 * i + 7]));
+              } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ac[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+              }
+            }
+            if (a.mode == kFwdLast)
+              *lrow = lse2_new * 0.69314718055994531f;
+            else
+              *lacc = lse2_new;
           }
-          a.lse[static_cast<long long>(a.lse_row[slot]) * a.S + qi] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
         }
       }
     }
@@ -342,13 +402,28 @@ cudaError_t run_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensor
 }  // namespace
 
 cudaError_t launch_attn_fwd(const AttnFwdDesc& d, int* status, cudaStream_t st) {
+  const int kv_len = d.kv_len ? d.kv_len : d.S;
+  const int kv_ld = d.kv_ld ? d.kv_ld : kv_len;
   if ((d.D != 64 && d.D != 128) || d.S % 128 || d.n_qslots <= 0 || d.n_qslots > kMaxSlots) return cudaErrorInvalidValue;
+  if (kv_len <= 0 || kv_len % 128 || kv_ld < kv_len || d.q_off < 0 || d.q_off % 128 || d.n_kvslots <= 0)
+    return cudaErrorInvalidValue;
+  if (d.mode < kFwdPlain || d.mode > kFwdLast || (d.mode != kFwdPlain && (!d.o_acc || !d.lse_acc)))
+    return cudaErrorInvalidValue;
+  for (int i = 0; i < d.n_qslots; ++i)
+    if (d.kv_slot[i] >= d.n_kvslots) return cudaErrorInvalidValue;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bf16(&tq, d.Q, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tk, d.K, d.D, (uint64_t)d.n_kvslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tv, d.V, d.D, (uint64_t)d.n_kvslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tk, d.K, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tv, d.V, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
   FwdArgs a;
   a.S = d.S;
+  a.kv_ld = kv_ld;
+  a.kv_blocks = kv_len / BKV;
+  a.q_off_blocks = d.q_off / BQ;
+  a.lse_ld = d.lse_ld ? d.lse_ld : d.S;
+  a.mode = d.mode;
+  a.o_acc = d.o_acc;
+  a.lse_acc = d.lse_acc;
   a.n_qslots = d.n_qslots;
   a.q_blocks = d.S / BQ;
   a.q_pairs = (a.q_blocks + 1) / 2;

@@ -41,21 +41,34 @@ struct GemmDesc {
   int split_k = 1;  // > 1 only with kOutF32Red: K is cut into split_k equal ranges
 };
 
+// Epilogues of the attention forward: one launch over all keys (plain), or
+// one of several launches over disjoint key chunks whose results merge by
+// log-sum-exp in an fp32 accumulator (first, middle, last; the last writes O
+// and lse).
+enum { kFwdPlain = 0, kFwdFirst = 1, kFwdMiddle = 2, kFwdLast = 3 };
+
 struct AttnFwdDesc {
   const void* Q = nullptr;  // [n_qslots][S][D] bf16
-  const void* K = nullptr;  // [n_kvslots][S][D] bf16
-  const void* V = nullptr;  // [n_kvslots][S][D] bf16
+  const void* K = nullptr;  // [n_kvslots][kv_ld][D] bf16, rows [0, kv_len) used
+  const void* V = nullptr;  // [n_kvslots][kv_ld][D] bf16
   void* O = nullptr;        // [n_qslots][S][D] bf16
-  float* lse = nullptr;     // rows lse_row[slot], each S long
+  float* lse = nullptr;     // rows lse_row[slot], lse_ld apart (natural log)
   int S = 0, D = 0, n_qslots = 0, n_kvslots = 0;
+  // Query row r sits at key position q_off + r (a multiple of 128, >= 0): it
+  // sees the keys at positions <= q_off + r below kv_len.  Defaults (0):
+  // kv_len = kv_ld = lse_ld = S, q_off = 0, the plain causal case.
+  int kv_len = 0, kv_ld = 0, q_off = 0, lse_ld = 0;
+  int mode = kFwdPlain;
+  float* o_acc = nullptr;    // [n_qslots][S][D] fp32 running output (merge modes)
+  float* lse_acc = nullptr;  // [n_qslots][S] fp32 running log-sum-exp, log2 units
   uint16_t kv_slot[kMaxSlots];
   uint16_t lse_row[kMaxSlots];
 };
 
 struct AttnBwdDesc {
   const void* Q = nullptr;   // [n_qslots][S][D] bf16
-  const void* K = nullptr;   // [n_kvslots][S][D] bf16
-  const void* V = nullptr;   // [n_kvslots][S][D] bf16
+  const void* K = nullptr;   // [n_kvslots][kv_ld][D] bf16, rows [0, kv_len) used
+  const void* V = nullptr;   // [n_kvslots][kv_ld][D] bf16
   const void* dO = nullptr;  // [n_qslots][S][D] bf16
   const float* lse2 = nullptr;  // [n_qslots][S]  minus the log-sum-exp in log2 units
   const float* Dsum = nullptr;  // [n_qslots][S]  rowsum(dO * O)
@@ -64,10 +77,12 @@ struct AttnBwdDesc {
   // (32 consecutive rows of one 4-wide column group contiguous, so one warp's
   // vector reduction covers a single 512-byte run)
   int dq_tiled = 0;
-  float* dK = nullptr;       // [n_kvslots][S][D] fp32
-  float* dV = nullptr;       // [n_kvslots][S][D] fp32
+  float* dK = nullptr;       // [n_kvslots][kv_ld][D] fp32
+  float* dV = nullptr;       // [n_kvslots][kv_ld][D] fp32
   int accumulate_kv = 0;     // add into dK/dV instead of overwriting
   int S = 0, D = 0, n_qslots = 0, n_kvslots = 0;
+  // key positions as in AttnFwdDesc (defaults: kv_len = kv_ld = S, q_off = 0)
+  int kv_len = 0, kv_ld = 0, q_off = 0;
   uint16_t kv_slot[kMaxSlots];  // q slot -> kv slot
 };
 
@@ -97,7 +112,8 @@ struct DqTiledDesc {
 struct BwdPrepDesc {
   const uint16_t* dO = nullptr; long long ld_do = 0;  // seq layout
   const uint16_t* O = nullptr; long long ld_o = 0;    // seq layout (saved forward output)
-  const float* lse = nullptr;                         // [*][S] natural log
+  const float* lse = nullptr;                         // [*][lse_ld] natural log
+  long long lse_ld = 0;                               // 0: S
   float* Dsum = nullptr;   // [n_slots][S]
   float* lse2 = nullptr;   // [n_slots][S]  -lse * log2(e)
   float* dQacc = nullptr;  // [n_slots][S][D], zeroed here

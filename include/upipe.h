@@ -91,6 +91,8 @@ typedef struct {
   int launches_by_kind[UPIPE_KERNEL_KINDS];
   double flops_by_kind[UPIPE_KERNEL_KINDS];
   double bytes_by_kind[UPIPE_KERNEL_KINDS];
+  size_t offload_bytes;           /* sequence-chunked calls: size of the offload store (0 otherwise) */
+  size_t offload_copy_bytes;      /* sequence-chunked calls: bytes copied between store and device */
 } upipe_stats;
 
 /* Workspace sizes in bytes for the layer calls (0 if the shape is invalid). */
@@ -144,6 +146,51 @@ int upipe_attn_bwd(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
                    int H, int G, int d_head, int U, int C, int sched, const upipe_bf16* O_saved,
                    const float* lse, const upipe_bf16* dY, upipe_bf16* dX, float* dW_qkv, float* dW_o, void* ws,
                    size_t ws_bytes, void* stream, upipe_stats* stats);
+
+/*
+ * Head stages combined with sequence chunks ("Untied Ulysses" summary page,
+ * paper.rainbus.top, sections Limitations and Future directions: FPDT chunks
+ * the sequence and keeps a memory edge through arbitrary chunk sizes, UPipe
+ * chunks the heads; the two are orthogonal and may be combined).  In-order
+ * schedule only.  The sequence is cut into n_chunks chunks of
+ * Sc = S / n_chunks tokens (Sc a multiple of 128 and of C).  Forward: for
+ * chunk i = 0, 1, ... and each stage, the chunk's rows are projected onto the
+ * stage's heads and exchanged; the stage's K and V of the chunk go to the
+ * offload store (one copy per KV head); the chunk's queries attend to KV
+ * chunks 0..i, fetched back from the store on a copy stream of the library,
+ * the partial softmax results merged by log-sum-exp; the stage's share of
+ * O W_o is added to the chunk's rows of Y.  Backward: all K/V chunks are
+ * recomputed into the store; query chunks run from the last to the first,
+ * partial dK/dV of each KV chunk are kept in the store until their own query
+ * chunk completes them.  Outputs and their layouts are those of
+ * upipe_attn_fwd / upipe_attn_bwd (same lse, O_saved; the two calls pair
+ * with each other only through them).
+ *   ws    : device, at least upipe_chunked_workspace_bytes() bytes, 256-byte
+ *           aligned; every buffer in it is O(Sc), none O(S).
+ *   store : device memory or page-locked host memory (cudaHostAlloc or
+ *           registered) of at least upipe_chunked_store_bytes() bytes,
+ *           16-byte aligned, owned by the caller: [chunk][K,V][G][Sc][d_head]
+ *           bf16 (forward), followed by the same in fp32 for dK, dV
+ *           (backward).  Its contents on return are scratch.
+ * The sizes return 0 for an invalid shape or chunk count.  Errors: as
+ * upipe_attn_fwd / upipe_attn_bwd; UPIPE_EINVAL for a bad chunk count or
+ * store pointer, UPIPE_ENOSPC for a short store; a failing copy gives
+ * UPIPE_ECUDA.  stats->offload_bytes and offload_copy_bytes report the
+ * store size and the bytes the call copied.
+ */
+size_t upipe_chunked_workspace_bytes(int S, int d_model, int H, int G, int d_head, int U, int C, int n_chunks,
+                                     int backward);
+size_t upipe_chunked_store_bytes(int S, int d_model, int H, int G, int d_head, int U, int C, int n_chunks,
+                                 int backward);
+int upipe_attn_fwd_chunked(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model,
+                           int H, int G, int d_head, int U, int C, int n_chunks, upipe_bf16* Y, upipe_bf16* O_saved,
+                           float* lse, void* ws, size_t ws_bytes, void* store, size_t store_bytes, void* stream,
+                           upipe_stats* stats);
+int upipe_attn_bwd_chunked(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model,
+                           int H, int G, int d_head, int U, int C, int n_chunks, const upipe_bf16* O_saved,
+                           const float* lse, const upipe_bf16* dY, upipe_bf16* dX, float* dW_qkv, float* dW_o,
+                           void* ws, size_t ws_bytes, void* store, size_t store_bytes, void* stream,
+                           upipe_stats* stats);
 
 /*
  * The Ulysses input all-to-all over C virtual ranks (Background, DeepSpeed
