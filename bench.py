@@ -261,16 +261,19 @@ def run_sweep(args):
     from synthetic import SHAPES
     dev = torch.device("cuda", 0)
     pk = peaks()
-    cases = []
+    cases = []  # (name, shape, schedule, sequence chunks (0: none), offload store)
     us = SHAPES["llama3_8b_256k_usweep"]
     for U in (8, 16, 32):
-        cases.append(("llama3_8b_256k_usweep", us.replace(U=U), 0))
+        cases.append(("llama3_8b_256k_usweep", us.replace(U=U), 0, 0, None))
     gq = SHAPES["llama3_8b_512k_gqa"]
-    cases += [("llama3_8b_512k_gqa", gq, 0), ("llama3_8b_512k_gqa", gq, 1)]
-    cases.append(("qwen3_32b_128k", SHAPES["qwen3_32b_128k"], 0))
+    cases += [("llama3_8b_512k_gqa", gq, 0, 0, None), ("llama3_8b_512k_gqa", gq, 1, 0, None)]
+    cases.append(("qwen3_32b_128k", SHAPES["qwen3_32b_128k"], 0, 0, None))
+    # head stages on sequence chunks, K/V offloaded to page-locked host memory
+    cases += [("llama3_8b_256k_chunked", us, 0, 8, "host"), ("llama3_8b_256k_chunked", us, 0, 16, "host"),
+              ("llama3_8b_512k_chunked", gq, 0, 16, "host")]
     if args.sweep_only:
         cases = [c for c in cases if c[0] in args.sweep_only.split(",")]
-    for name, sh, sched in cases:
+    for name, sh, sched, n_chunks, where in cases:
         s = upipe.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, sh.U, sh.C, sched)
         g = torch.Generator(device=dev).manual_seed(0)
         w_std = 1.0 / np.sqrt(sh.d_model)
@@ -279,10 +282,29 @@ def run_sweep(args):
             return (torch.randn(*shape, generator=g, device=dev) * std).to(torch.bfloat16)
         X, dY = randn(sh.S, sh.d_model), randn(sh.S, sh.d_model)
         Wqkv, Wo = randn(sh.d_model, sh.qkv_cols, std=w_std), randn(sh.H * sh.d_head, sh.d_model, std=w_std)
-        wsf = torch.empty(upipe.fwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
-        wsb = torch.empty(upipe.bwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
-        Y, O, lse, _ = upipe.attn_fwd(X, Wqkv, Wo, s, ws=wsf)
-        dX, dWqkv, dWo, _ = upipe.attn_bwd(X, Wqkv, Wo, O, lse, dY, s, ws=wsb)
+        store = None
+        if n_chunks:
+            wsf = torch.empty(upipe.chunked_workspace_bytes(s, n_chunks, False), dtype=torch.uint8, device=dev)
+            wsb = torch.empty(upipe.chunked_workspace_bytes(s, n_chunks, True), dtype=torch.uint8, device=dev)
+            store = torch.empty(upipe.chunked_store_bytes(s, n_chunks, True), dtype=torch.uint8)
+            store = store.pin_memory() if where == "host" else store.to(dev)
+
+            def fwd(**kw):
+                return upipe.attn_fwd_chunked(X, Wqkv, Wo, s, n_chunks, store, ws=wsf, **kw)
+
+            def bwd(O, lse, **kw):
+                return upipe.attn_bwd_chunked(X, Wqkv, Wo, O, lse, dY, s, n_chunks, store, ws=wsb, **kw)
+        else:
+            wsf = torch.empty(upipe.fwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
+            wsb = torch.empty(upipe.bwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
+
+            def fwd(**kw):
+                return upipe.attn_fwd(X, Wqkv, Wo, s, ws=wsf, **kw)
+
+            def bwd(O, lse, **kw):
+                return upipe.attn_bwd(X, Wqkv, Wo, O, lse, dY, s, ws=wsb, **kw)
+        Y, O, lse, _ = fwd()
+        dX, dWqkv, dWo, _ = bwd(O, lse)
         torch.cuda.synchronize()
         clocks = ClockSampler(0)
         clocks.start()
@@ -291,8 +313,8 @@ def run_sweep(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(args.sweep_steps):
-            _, _, _, stf = upipe.attn_fwd(X, Wqkv, Wo, s, Y=Y, O_saved=O, lse=lse, ws=wsf)
-            _, _, _, stb = upipe.attn_bwd(X, Wqkv, Wo, O, lse, dY, s, dX=dX, dW_qkv=dWqkv, dW_o=dWo, ws=wsb)
+            _, _, _, stf = fwd(Y=Y, O_saved=O, lse=lse)
+            _, _, _, stb = bwd(O, lse, dX=dX, dW_qkv=dWqkv, dW_o=dWo)
         e1.record()
         torch.cuda.synchronize()
         clk = clocks.stop()
@@ -310,8 +332,11 @@ def run_sweep(args):
             "ulysses_form_12SHd": 12 * sh.S * sh.H * sh.d_head,
             "permute_bytes_fwd": stf["permute_bytes"], "permute_bytes_bwd": stb["permute_bytes"],
             "persistent_bytes": stf["persistent_bytes"], "steps": args.sweep_steps, "clocks": clk,
+            "workspace_fwd_bytes": wsf.numel(), "workspace_bwd_bytes": wsb.numel(),
+            "sequence_chunks": n_chunks, "offload_store": where, "offload_bytes": stb["offload_bytes"],
+            "offload_copy_bytes": stf["offload_copy_bytes"] + stb["offload_copy_bytes"],
             "kernel_ms_per_step": {k: v[0] / args.sweep_steps for k, v in prof.items()}}), flush=True)
-        del X, dY, Wqkv, Wo, wsf, wsb, Y, O, lse, dX, dWqkv, dWo
+        del X, dY, Wqkv, Wo, wsf, wsb, Y, O, lse, dX, dWqkv, dWo, store, fwd, bwd
         torch.cuda.empty_cache()
     return 0
 

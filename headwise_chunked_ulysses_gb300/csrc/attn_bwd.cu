@@ -41,6 +41,7 @@ constexpr int CH = 128 * 128;  // a 64-column chunk of a 128-row bf16 tile
 struct BwdArgs {
   int S, n_qslots, n_kvslots, q_blocks;
   int kv_ld, kv_blocks, q_off_blocks;  // key positions: see AttnBwdDesc
+  int q_split;  // CTAs per KV block, each a contiguous share of its items (dK, dV added atomically)
   float scale_log2, scale;
   int accumulate_kv;
   int dq_tiled;
@@ -78,11 +79,23 @@ struct BwdCfg {
 // b + q_off_blocks).
 struct ItemCursor {
   int qs = -1, qb = 0, qb_first = 0, q_blocks = 0;
+  bool primed = false;
   __device__ bool next(const BwdArgs& a, int kvs) {
+    if (primed) { primed = false; return true; }
     if (qs >= 0 && ++qb < q_blocks) return true;
     for (++qs; qs < a.n_qslots; ++qs)
       if (a.kv_slot[qs] == kvs) { qb = qb_first; return true; }
     return false;
+  }
+  // position on item k (0-based) of this KV slot; next() then returns it first
+  __device__ void seek(const BwdArgs& a, int kvs, int k) {
+    const int per_slot = q_blocks - qb_first;
+    if (k <= 0 || per_slot <= 0) return;
+    int skip = k / per_slot;
+    for (qs = 0; qs < a.n_qslots; ++qs)
+      if (a.kv_slot[qs] == kvs && skip-- == 0) break;
+    qb = qb_first + k % per_slot;
+    primed = true;
   }
 };
 
@@ -118,14 +131,19 @@ __global__ void __launch_bounds__(512, 1)
   // (most work) first, so the CTAs running at one time share few slots'
   // query-side data
   const int grp_slots = a.grp_slots;
+  // (the q_split CTAs of one KV block are adjacent in launch order)
+  const int part = static_cast<int>(blockIdx.x) % a.q_split;
+  const int cta = static_cast<int>(blockIdx.x) / a.q_split;
   const int per_grp = grp_slots * a.kv_blocks;
-  const int grp = static_cast<int>(blockIdx.x) / per_grp, rem = static_cast<int>(blockIdx.x) % per_grp;
+  const int grp = cta / per_grp, rem = cta % per_grp;
   const int kvb = rem / grp_slots;
   const int kvs = grp * grp_slots + rem % grp_slots;
   int n_q = 0;
   for (int i = 0; i < a.n_qslots; ++i) n_q += (a.kv_slot[i] == kvs);
   const int qb_first = max(0, kvb - a.q_off_blocks);
-  const int n_items = n_q * max(0, a.q_blocks - qb_first);
+  const int n_all = n_q * max(0, a.q_blocks - qb_first);
+  const int item0 = static_cast<int>(static_cast<long long>(n_all) * part / a.q_split);
+  const int n_items = static_cast<int>(static_cast<long long>(n_all) * (part + 1) / a.q_split) - item0;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -170,6 +188,7 @@ __global__ void __launch_bounds__(512, 1)
       ItemCursor cur;
       cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
+      cur.seek(a, kvs, item0);
       for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
         const int st = i & 1;
         if (!mbar_wait(&qdo_empty[st], ((i >> 1) & 1) ^ 1, w, 40)) break;
@@ -271,6 +290,7 @@ __global__ void __launch_bounds__(512, 1)
       ItemCursor cur;
       cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
+      cur.seek(a, kvs, item0);
       bool ok = true;
       int i = 0;
       for (; i < n_items && cur.next(a, kvs); ++i) {
@@ -359,6 +379,10 @@ __global__ void __launch_bounds__(512, 1)
             for (int e = 0; e < 8; ++e) {
               float4 x = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
                                      __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
+              if (a.q_split > 1) {  // other CTAs add to the same rows
+                red_add_v4(dst + c * 32 + 4 * e, x.x, x.y, x.z, x.w);
+                continue;
+              }
               if (a.accumulate_kv) {
                 const float4 p = o[e];
                 x.x += p.x; x.y += p.y; x.z += p.z; x.w += p.w;
@@ -378,6 +402,7 @@ __global__ void __launch_bounds__(512, 1)
       ItemCursor cur;
       cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
+      cur.seek(a, kvs, item0);
       for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
         if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
         tc_fence_after();
@@ -402,7 +427,7 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
     }
-  } else if (aligned && n_items == 0 && !a.accumulate_kv && warp >= 4 && warp < 12) {
+  } else if (aligned && n_items == 0 && !a.accumulate_kv && a.q_split == 1 && warp >= 4 && warp < 12) {
     // a KV slot no query head uses in this launch: its gradient is zero
     const int row = (warp & 3) * 32 + lane;
     const int half = (warp - 4) >> 2;
@@ -488,7 +513,7 @@ cudaError_t run_bwd(const CUtensorMap* tm, const BwdArgs& args, cudaStream_t st)
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<args.n_kvslots * args.kv_blocks, 512, BwdCfg<D>::SMEM, st>>>(tm[0], tm[1], tm[2], tm[3], args);
+  kern<<<args.n_kvslots * args.kv_blocks * args.q_split, 512, BwdCfg<D>::SMEM, st>>>(tm[0], tm[1], tm[2], tm[3], args);
   return cudaGetLastError();
 }
 
@@ -517,6 +542,7 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) 
       d.n_kvslots <= 0)
     return cudaErrorInvalidValue;
   if (kv_len <= 0 || kv_len % 128 || kv_ld < kv_len || d.q_off < 0 || d.q_off % 128) return cudaErrorInvalidValue;
+  if (d.q_split < 1 || d.q_split > 16) return cudaErrorInvalidValue;
   for (int i = 0; i < d.n_qslots; ++i)
     if (d.kv_slot[i] >= d.n_kvslots) return cudaErrorInvalidValue;
   CUtensorMap tm[4];
@@ -529,6 +555,7 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) 
   a.kv_ld = kv_ld;
   a.kv_blocks = kv_len / BKV;
   a.q_off_blocks = d.q_off / BQ;
+  a.q_split = d.q_split;
   a.n_qslots = d.n_qslots;
   a.n_kvslots = d.n_kvslots;
   a.q_blocks = d.S / BQ;

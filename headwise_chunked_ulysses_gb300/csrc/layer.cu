@@ -812,6 +812,23 @@ struct ChunkPlan {
   size_t arena = 0, persistent = 0, total = 0, store = 0;
 };
 
+// CTAs per KV block of a chunk-pair attention backward: the split (1..8)
+// whose grid fills its last wave of SMs best (ties to the smaller split)
+int choose_q_split(long long ctas) {
+  const double sms = num_sms();
+  int best = 1;
+  double best_eff = 0.0;
+  for (int q = 1; q <= 8; ++q) {
+    const double waves = static_cast<double>(ctas) * q / sms;
+    const double eff = waves / std::ceil(waves);
+    if (eff > best_eff + 0.02) {
+      best = q;
+      best_eff = eff;
+    }
+  }
+  return best;
+}
+
 int check_chunks(const Shape& s, int n_c) {
   int rc = check_shape(s);
   if (rc != UPIPE_OK) return rc;
@@ -1216,6 +1233,7 @@ int attn_bwd_chunked_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const u
       ab.S = Sc; ab.D = d; ab.n_qslots = U; ab.n_kvslots = nkv;
       ab.kv_len = Sc; ab.kv_ld = Sc;
       ab.accumulate_kv = acc ? 1 : 0;
+      ab.q_split = choose_q_split(static_cast<long long>(nkv) * (Sc / 128));
       for (int k = 0; k < U; ++k)
         ab.kv_slot[k] = static_cast<uint16_t>(std::find(g.kv_proj.begin(), g.kv_proj.end(), kv_of(s, g.q_heads[k])) -
                                               g.kv_proj.begin());
@@ -1225,6 +1243,9 @@ int attn_bwd_chunked_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const u
         uint16_t* kw = reinterpret_cast<uint16_t*>(w + c.off_kvw[b]);
         float* dkw = reinterpret_cast<float*>(w + c.off_dkvw[b]);
         cst.wait(L.st, cst.ready()[b]);
+        if (ab.q_split > 1 && !acc && L.ok() &&
+            cudaMemsetAsync(dkw, 0, static_cast<size_t>(2 * nkv) * chunk_elems * 4, L.st) != cudaSuccess)
+          L.err = cudaErrorUnknown;  // the split CTAs add their dK, dV into zeros
         ab.K = kw;
         ab.V = kw + static_cast<size_t>(nkv) * chunk_elems;
         ab.dK = dkw;

@@ -83,6 +83,11 @@ struct AttnBwdDesc {
   int S = 0, D = 0, n_qslots = 0, n_kvslots = 0;
   // key positions as in AttnFwdDesc (defaults: kv_len = kv_ld = S, q_off = 0)
   int kv_len = 0, kv_ld = 0, q_off = 0;
+  // CTAs per KV block (1..16), each taking a contiguous share of the block's
+  // (query slot, query block) items; above 1, dK and dV are ADDED atomically
+  // into buffers that hold zeros or earlier partial sums (accumulate_kv is
+  // then implied and nothing is zero-filled)
+  int q_split = 1;
   uint16_t kv_slot[kMaxSlots];  // q slot -> kv slot
 };
 

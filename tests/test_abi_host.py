@@ -211,3 +211,46 @@ def test_prefetch_workspace_adds_one_stage_set(upipe, name, sched):
     extra = pf - base
     assert extra >= head_slots * slot
     assert extra <= head_slots * slot + 3 * s.U * slot + 2 * 256  # + the sequence buffer (<= U + 2 U heads)
+
+
+@pytest.mark.parametrize("name,n_chunks", [("tiny", 1), ("tiny", 4), ("tiny", 8), ("llama3_8b_32k", 4),
+                                           ("llama3_8b_256k_usweep", 8), ("qwen3_32b_128k", 16)])
+@pytest.mark.parametrize("U", [None, 1])
+def test_chunked_workspace_follows_its_closed_form(upipe, name, n_chunks, U):
+    """Head stages on sequence chunks: every device buffer is a chunk of
+    Sc = S / n_chunks tokens.  Forward: the sequence-layout stage buffer and the
+    head-layout Q, K, V (2 bytes each, U + 2 kv heads), two K/V windows (2 kv
+    heads each), the fp32 output accumulator and its log-sum-exp: 8 (U + 2 kv)
+    Sc d + 4 U Sc d + 4 U Sc, plus the fp32 chunk of Y when there is more than
+    one stage.  Backward: the stage buffer (2 (U + 2 kv)), head-layout Q and dO
+    (2 + 2 per slot), two K/V and two fp32 dK/dV windows (4 + 8 per kv head
+    each), D and lse (4 + 4) and fp32 dQ (4 per slot).  Store: K, V of every KV
+    head over all S (2 + 2 bytes), plus fp32 dK, dV (backward)."""
+    from synthetic import SHAPES
+    s = SHAPES[name]
+    u = s.U if U is None else U
+    sh = upipe.Shape(s.S, s.d_model, s.H, s.G, s.d_head, u, s.C if u % s.C == 0 else 1, upipe.IN_ORDER)
+    Sc, d = s.S // n_chunks, s.d_head
+    kv = max(1, u * s.G // s.H)
+    acc = Sc * s.d_model * 4 if s.H // u > 1 else 0
+    fwd = 2 * Sc * d * (u + 2 * kv) * 2 + 2 * (2 * kv * Sc * d * 2) + 4 * u * Sc * d + 4 * u * Sc
+    bwd = (2 * Sc * d * (u + 2 * kv) + 2 * u * Sc * d + 2 * (2 * kv * Sc * d * 2) + 2 * (2 * kv * Sc * d * 4)
+           + 2 * u * Sc * d + 8 * u * Sc + 4 * u * Sc * d)
+    got_f = upipe.chunked_workspace_bytes(sh, n_chunks, False) - acc
+    got_b = upipe.chunked_workspace_bytes(sh, n_chunks, True) - acc
+    assert 0 <= got_f - fwd <= 6 * 256
+    assert 0 <= got_b - bwd <= 10 * 256
+    assert upipe.chunked_store_bytes(sh, n_chunks, False) == 4 * s.G * s.S * d
+    assert upipe.chunked_store_bytes(sh, n_chunks, True) == 12 * s.G * s.S * d
+
+
+def test_chunked_sizes_reject_bad_chunk_counts(upipe):
+    sh = upipe.Shape(1024, 512, 8, 2, 64, 2, 2, upipe.IN_ORDER)
+    for n in (0, -1, 3, 16, 1024):  # no split, not dividing S, chunks under 128 tokens
+        assert upipe.chunked_workspace_bytes(sh, n, False) == 0
+        assert upipe.chunked_store_bytes(sh, n, True) == 0
+    odd = upipe.Shape(3072, 512, 12, 3, 64, 6, 3, upipe.IN_ORDER)  # 3 ranks
+    assert upipe.chunked_workspace_bytes(odd, 3, False) == 0     # 1024-token chunks do not split over 3 ranks
+    assert upipe.chunked_workspace_bytes(odd, 8, False) > 0      # 384-token chunks do (128 each)
+    gqa = upipe.Shape(1024, 512, 8, 2, 64, 2, 2, upipe.GQA_OUT_OF_ORDER)
+    assert upipe.chunked_workspace_bytes(gqa, 2, False) > 0      # the schedule argument is not taken: in order
