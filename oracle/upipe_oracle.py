@@ -612,6 +612,92 @@ def chunked_backward(X, W_qkv, W_o, H, G, d_head, U, C, n_chunks, dY, O_saved, l
 
 
 # ---------------------------------------------------------------------------
+# lower-precision heads ([U1] weaknesses from an independent analysis: some
+# heads could run in FP8 to cut memory and communication further)
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+FP8_BLOCK = 128  # keys per K scale
+
+
+def e4m3_round(x):
+    """Nearest value of the FP8 E4M3 format (1 sign, 4 exponent bits with
+    bias 7, 3 mantissa bits; no infinities; largest finite 448; subnormals
+    m * 2^-9), ties to the even mantissa, saturating at +-448."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    # spacing of the format around |x|: 2^(e-3) in binade [2^e, 2^(e+1)), e >= -6
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)
+    q = 2.0 ** (e - 3)
+    r = np.round(a / q) * q  # numpy rounds half to even, and a/q is exact
+    r = np.minimum(r, E4M3_MAX)
+    return np.where(a > 0, np.sign(x) * r, 0.0 * x)
+
+
+def fp8_scale(amax):
+    """Per-group scale: amax / 448 in fp32 (1 for an all-zero group)."""
+    amax = np.float32(amax)
+    return np.float32(1.0) if amax == 0 else np.float32(amax / np.float32(E4M3_MAX))
+
+
+def quantize_e4m3(x, scale):
+    """Codes of x (fp32 values) under one fp32 scale: e4m3(fl32(x / scale)),
+    returned as their values (exact in fp64)."""
+    return e4m3_round(np.asarray(x, dtype=np.float32) / np.float32(scale))
+
+
+def fp8_rows(q):
+    """Q of one head [S, d] -> (codes [S, d], scales [S]): one scale per row."""
+    sc = np.array([fp8_scale(np.abs(np.float32(r)).max()) for r in np.asarray(q, dtype=np.float32)], dtype=np.float32)
+    return np.stack([quantize_e4m3(r, s) for r, s in zip(np.asarray(q, dtype=np.float32), sc)]), sc
+
+
+def fp8_key_blocks(k):
+    """K of one head [S, d] -> (codes, scales [S / 128]): one scale per block of
+    128 consecutive keys."""
+    k = np.asarray(k, dtype=np.float32)
+    codes, scales = np.zeros(k.shape), []
+    for b in range(0, k.shape[0], FP8_BLOCK):
+        s = fp8_scale(np.abs(k[b:b + FP8_BLOCK]).max())
+        codes[b:b + FP8_BLOCK] = quantize_e4m3(k[b:b + FP8_BLOCK], s)
+        scales.append(s)
+    return codes, np.array(scales, dtype=np.float32)
+
+
+def attention_head_forward_fp8(q, k, v):
+    """Causal attention whose scores use FP8 Q and K: q = codes * row scale,
+    k = codes * block scale, then the exact softmax and P V.  Returns (O, lse)."""
+    cq, sq = fp8_rows(q)
+    ck, sk = fp8_key_blocks(k)
+    qd = cq * sq.astype(np.float64)[:, None]
+    kd = ck * np.repeat(sk.astype(np.float64), FP8_BLOCK)[:k.shape[0], None]
+    o, lse, _ = attention_head_forward(qd, kd, v)
+    return o, lse
+
+
+def layer_forward_fp8(X, W_qkv, W_o, H, G, d_head, fp8_heads):
+    """``layer_forward`` with the heads in fp8_heads attending through FP8
+    Q and K (``attention_head_forward_fp8``); other heads are unchanged."""
+    S = X.shape[0]
+    d = d_head
+    Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
+    K = [X @ Wk[g] for g in range(G)]
+    V = [X @ Wv[g] for g in range(G)]
+    O = np.zeros((S, H * d))
+    lse = np.zeros((H, S))
+    for h in range(H):
+        g = kv_head(h, H, G)
+        if h in fp8_heads:
+            o, l = attention_head_forward_fp8(X @ Wq[h], K[g], V[g])
+        else:
+            o, l, _ = attention_head_forward(X @ Wq[h], K[g], V[g])
+        O[:, h * d:(h + 1) * d] = o
+        lse[h] = l
+    return O @ W_o, O, lse
+
+
+# ---------------------------------------------------------------------------
 # FLOP accounting (model FLOPs; not a method step)
 # ---------------------------------------------------------------------------
 

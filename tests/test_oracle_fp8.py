@@ -1,0 +1,160 @@
+"""Pins of the oracle's FP8 (E4M3) heads.
+
+The E4M3 rounding is pinned to the format's definition (every code decoded
+from its bit fields is a fixed point; midpoints go to the even mantissa;
+overflow saturates) and to torch's own float8_e4m3fn conversion.  The FP8
+attention is pinned to the exact attention when Q and K are already FP8 values
+under power-of-two scales, and to the plain layer within the error the
+format's 3-bit mantissa allows.  Planted slips (truncation, a wrong exponent
+bias, a missing scale) must fail a pin.
+"""
+import numpy as np
+import pytest
+
+from oracle import upipe_oracle as orc
+
+
+def _all_e4m3_values():
+    """Every finite E4M3 value from the bit fields: (-1)^s 2^(e-7) (1 + m/8),
+    e = 1..15, with e = 15, m = 7 the NaN; subnormals 2^-6 m/8."""
+    vals = []
+    for e in range(16):
+        for m in range(8):
+            if e == 15 and m == 7:
+                continue
+            v = 2.0 ** -6 * m / 8 if e == 0 else 2.0 ** (e - 7) * (1 + m / 8)
+            vals += [v, -v]
+    return np.array(sorted(set(vals)))
+
+
+def test_every_code_is_a_fixed_point():
+    v = _all_e4m3_values()
+    assert len(v) == 253  # 2 x 126 nonzero magnitudes + one zero
+    assert v.max() == 448.0
+    assert np.array_equal(orc.e4m3_round(v), v)
+
+
+def test_midpoints_round_to_even_and_overflow_saturates():
+    v = _all_e4m3_values()
+    pos = v[v >= 0]
+    mid = (pos[:-1] + pos[1:]) / 2
+    got = orc.e4m3_round(mid)
+    lo, hi = pos[:-1], pos[1:]
+    # the even neighbour has an even mantissa code: its index among positives is even
+    idx_lo = np.arange(len(lo))
+    want = np.where(idx_lo % 2 == 0, lo, hi)
+    assert np.array_equal(got, want)
+    assert np.array_equal(orc.e4m3_round(np.array([449.0, 464.0, 1e6, -1e6])), [448.0, 448.0, 448.0, -448.0])
+    assert orc.e4m3_round(np.array([2.0 ** -10]))[0] == 0.0  # half the smallest subnormal: to even (0)
+
+
+def test_rounding_matches_torch_float8():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8 in this torch")
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal(20000) * np.exp(rng.uniform(-14, 6, 20000))
+    x = x[np.abs(x) < 448]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(orc.e4m3_round(x), want)
+
+
+def test_fp8_attention_is_exact_on_fp8_inputs():
+    """Q rows and K blocks whose amax is exactly 448 * 2^k and whose entries are
+    E4M3 values times 2^k quantize to themselves: the FP8 attention is then the
+    exact attention of those inputs."""
+    rng = np.random.default_rng(1)
+    v_all = _all_e4m3_values()
+    S, d = 256, 16
+    q = rng.choice(v_all, size=(S, d)) / 8.0
+    k = rng.choice(v_all, size=(S, d)) / 4.0
+    q[:, 0] = 448.0 / 8.0
+    k[::128, 0] = 448.0 / 4.0
+    v = rng.standard_normal((S, d))
+    o8, l8 = orc.attention_head_forward_fp8(q, k, v)
+    o, l, _ = orc.attention_head_forward(q, k, v)
+    assert np.abs(o8 - o).max() < 1e-13 and np.abs(l8 - l).max() < 1e-13
+
+
+def test_fp8_scales_follow_rows_and_key_blocks():
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((256, 8)).astype(np.float32)
+    codes, sc = orc.fp8_rows(q)
+    assert sc.shape == (256,) and np.abs(codes).max() <= 448
+    assert np.allclose(np.abs(codes).max(axis=1), 448.0)  # each row's largest entry maps to the top code
+    kc, ks = orc.fp8_key_blocks(q)
+    assert ks.shape == (2,)
+    assert np.isclose(np.abs(kc[:128]).max(), 448.0) and np.isclose(np.abs(kc[128:]).max(), 448.0)
+    z, zs = orc.fp8_rows(np.zeros((4, 8), np.float32))
+    assert (z == 0).all() and (zs == 1).all()
+
+
+def _layer_gap(fp8_heads):
+    rng = np.random.default_rng(3)
+    S, dm, H, G, d = 256, 32, 4, 2, 16
+    X = rng.standard_normal((S, dm))
+    W_qkv = rng.standard_normal((dm, (H + 2 * G) * d)) / np.sqrt(dm)
+    W_o = rng.standard_normal((H * d, dm)) / np.sqrt(dm)
+    Y, O, lse = orc.layer_forward(X, W_qkv, W_o, H, G, d)
+    Y8, O8, lse8 = orc.layer_forward_fp8(X, W_qkv, W_o, H, G, d, fp8_heads)
+    per_head = [np.linalg.norm(O8[:, h * d:(h + 1) * d] - O[:, h * d:(h + 1) * d]) /
+                np.linalg.norm(O[:, h * d:(h + 1) * d]) for h in range(H)]
+    return per_head, np.linalg.norm(Y8 - Y) / np.linalg.norm(Y)
+
+
+def test_fp8_heads_stay_within_the_format_error_and_others_are_untouched():
+    per_head, gy = _layer_gap({1, 2})
+    assert per_head[0] == 0.0 and per_head[3] == 0.0
+    # 3 mantissa bits: relative rounding error <= 2^-4 per entry; the scores'
+    # error is an average of d such errors, and softmax and P V average again
+    assert 1e-4 < per_head[1] < 5e-2 and 1e-4 < per_head[2] < 5e-2
+    assert gy < 5e-2
+
+
+def _truncate(x):
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    e = np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), -6.0)
+    q = 2.0 ** (e - 3)
+    return np.sign(x) * np.minimum(np.floor(a / q) * q, 448.0)
+
+
+def _wrong_bias(x):
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    e = np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), -7.0)
+    q = 2.0 ** (e - 3)
+    return np.sign(x) * np.minimum(np.round(a / q) * q, 448.0)
+
+
+@pytest.mark.parametrize("fn", [_truncate, _wrong_bias])
+def test_planted_rounding_slips_fail_the_pins(monkeypatch, fn):
+    monkeypatch.setattr(orc, "e4m3_round", fn)
+    v = _all_e4m3_values()
+    pos = v[v >= 0]
+    mid = (pos[:-1] + pos[1:]) / 2
+    fixed = np.array_equal(orc.e4m3_round(v), v)
+    idx_lo = np.arange(len(mid))
+    mids_ok = np.array_equal(orc.e4m3_round(mid), np.where(idx_lo % 2 == 0, pos[:-1], pos[1:]))
+    assert not (fixed and mids_ok)
+
+
+def _scale_gap():
+    """Q entries near 3e-3 and K entries near 3e3: without per-group scales Q
+    falls into E4M3's subnormals and K saturates at 448."""
+    rng = np.random.default_rng(1)
+    q = rng.standard_normal((128, 8)) * 3e-3
+    k = rng.standard_normal((128, 8)) * 3e3
+    v = rng.standard_normal((128, 8))
+    o, _, _ = orc.attention_head_forward(q, k, v)
+    o8, _ = orc.attention_head_forward_fp8(q, k, v)
+    return np.linalg.norm(o8 - o) / np.linalg.norm(o)
+
+
+def test_scales_keep_small_and_large_heads_in_range():
+    assert _scale_gap() < 0.2
+
+
+def test_planted_missing_scale_fails_the_pin(monkeypatch):
+    monkeypatch.setattr(orc, "fp8_scale", lambda amax: np.float32(1.0))
+    assert _scale_gap() > 0.5
