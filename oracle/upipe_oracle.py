@@ -635,6 +635,16 @@ def e4m3_round(x):
     return np.where(a > 0, np.sign(x) * r, 0.0 * x)
 
 
+def bf16_round(x):
+    """Nearest bfloat16 value (8 exponent bits, 7 mantissa bits), ties to the
+    even mantissa: the top 16 bits of the fp32 pattern after adding half a
+    unit of the dropped 16 bits (plus the kept LSB for ties).  x is rounded to
+    fp32 first."""
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def fp8_scale(amax):
     """Per-group scale: amax / 448 in fp32 (1 for an all-zero group)."""
     amax = np.float32(amax)
@@ -678,7 +688,10 @@ def attention_head_forward_fp8(q, k, v):
 
 def layer_forward_fp8(X, W_qkv, W_o, H, G, d_head, fp8_heads):
     """``layer_forward`` with the heads in fp8_heads attending through FP8
-    Q and K (``attention_head_forward_fp8``); other heads are unchanged."""
+    Q and K (``attention_head_forward_fp8``); other heads are unchanged.  The
+    codes are decided from the projections as the exchange holds them, in
+    bf16: a quantised code is an integer the two sides must decide from the
+    same value."""
     S = X.shape[0]
     d = d_head
     Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
@@ -689,7 +702,7 @@ def layer_forward_fp8(X, W_qkv, W_o, H, G, d_head, fp8_heads):
     for h in range(H):
         g = kv_head(h, H, G)
         if h in fp8_heads:
-            o, l = attention_head_forward_fp8(X @ Wq[h], K[g], V[g])
+            o, l = attention_head_forward_fp8(bf16_round(X @ Wq[h]), bf16_round(K[g]), V[g])
         else:
             o, l, _ = attention_head_forward(X @ Wq[h], K[g], V[g])
         O[:, h * d:(h + 1) * d] = o

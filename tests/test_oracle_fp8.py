@@ -111,6 +111,17 @@ def test_fp8_heads_stay_within_the_format_error_and_others_are_untouched():
     assert gy < 5e-2
 
 
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal(50000) * np.exp(rng.uniform(-30, 30, 50000))).astype(np.float32)
+    x[:4] = [0.0, -0.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8]  # ties: to even (down, then up)
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = orc.bf16_round(x)
+    assert np.array_equal(got, want)
+    assert got[2] == 1.0 and got[3] == 1.0 + 2.0 ** -6
+
+
 def _truncate(x):
     x = np.asarray(x, dtype=np.float64)
     a = np.abs(x)
