@@ -29,6 +29,7 @@ EXPORTS = (
     "upipe_sync_status", "upipe_status_str", "upipe_version", "upipe_profile_enable", "upipe_profile_read",
     "upipe_graphs_enable", "upipe_chunked_workspace_bytes", "upipe_chunked_store_bytes",
     "upipe_attn_fwd_chunked", "upipe_attn_bwd_chunked",
+    "upipe_quantize_e4m3", "upipe_attention_fwd_fp8", "upipe_attn_fwd_fp8",
 )
 
 
@@ -83,6 +84,9 @@ def _sig(lib):
         "upipe_version": (I, []),
         "upipe_profile_enable": (I, [I]),
         "upipe_graphs_enable": (I, [I]),
+        "upipe_quantize_e4m3": (I, [P, I, I, I, LL, I, P, P, P]),
+        "upipe_attention_fwd_fp8": (I, [P, P, P, P, P, I, I, I, I, i32p, P, P, P]),
+        "upipe_attn_fwd_fp8": (I, [P, P, P] + [I] * 7 + [ctypes.c_char_p, P, P, P, P, Z, P, P]),
         "upipe_chunked_workspace_bytes": (Z, [I] * 9),
         "upipe_chunked_store_bytes": (Z, [I] * 9),
         "upipe_attn_fwd_chunked": (I, [P, P, P] + [I] * 8 + [P, P, P, P, Z, P, Z, P, P]),
@@ -229,6 +233,60 @@ def attn_bwd(X, W_qkv, W_o, O_saved, lse, dY, sh: Shape, dX=None, dW_qkv=None, d
         _ptr(dX, bf, "dX"), _ptr(dW_qkv, f32, "dW_qkv"), _ptr(dW_o, f32, "dW_o"),
         _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(st)))
     return dX, dW_qkv, dW_o, st.as_dict()
+
+
+def quantize_e4m3(src, S, n_heads, d_head, src_row_stride, per_row, dst=None, scales=None, stream=None):
+    """E4M3 codes [n_heads, S, d_head] (uint8) and fp32 scales of bf16 rows in
+    sequence layout (see upipe_quantize_e4m3).  Returns (codes, scales)."""
+    torch = _torch()
+    dev = src.device
+    dst = torch.empty(n_heads, S, d_head, dtype=torch.uint8, device=dev) if dst is None else dst
+    n_sc = S if per_row else S // 128
+    scales = torch.empty(n_heads, n_sc, dtype=torch.float32, device=dev) if scales is None else scales
+    _check("upipe_quantize_e4m3", lib().upipe_quantize_e4m3(
+        _ptr(src, torch.bfloat16, "src"), S, n_heads, d_head, src_row_stride, 1 if per_row else 0,
+        _ptr(dst, torch.uint8, "dst"), _ptr(scales, torch.float32, "scales"), _stream(stream)))
+    return dst, scales
+
+
+def attention_fwd_fp8(Q8, q_scale, K8, k_scale, V, kv_of_q, O=None, lse=None, stream=None):
+    """Attention with FP8 scores (see upipe_attention_fwd_fp8).  Returns (O, lse)."""
+    torch = _torch()
+    n_q, S, d = Q8.shape
+    n_kv = K8.shape[0]
+    O = torch.empty(n_q, S, d, dtype=torch.bfloat16, device=Q8.device) if O is None else O
+    lse = torch.empty(n_q, S, dtype=torch.float32, device=Q8.device) if lse is None else lse
+    kv = (ctypes.c_int32 * n_q)(*kv_of_q)
+    _check("upipe_attention_fwd_fp8", lib().upipe_attention_fwd_fp8(
+        _ptr(Q8, torch.uint8, "Q"), _ptr(q_scale, torch.float32, "q_scale"), _ptr(K8, torch.uint8, "K"),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(V, torch.bfloat16, "V"), n_q, n_kv, S, d, kv,
+        _ptr(O, torch.bfloat16, "O"), _ptr(lse, torch.float32, "lse"), _stream(stream)))
+    return O, lse
+
+
+def attn_fwd_fp8(X, W_qkv, W_o, sh: Shape, fp8_heads, Y=None, O_saved=None, lse=None, ws=None, stream=None):
+    """Layer forward (in-order stages) with FP8 scores for the heads in
+    fp8_heads (a set of head indices; whole stages).  Returns (Y, O_saved,
+    lse, stats)."""
+    torch = _torch()
+    bf, f32 = torch.bfloat16, torch.float32
+    dev = X.device
+    S, dm, H, d = sh.S, sh.d_model, sh.H, sh.d_head
+    Y = torch.empty(S, dm, dtype=bf, device=dev) if Y is None else Y
+    O_saved = torch.empty(S, H * d, dtype=bf, device=dev) if O_saved is None else O_saved
+    lse = torch.empty(H, S, dtype=f32, device=dev) if lse is None else lse
+    s0 = Shape(*sh.args()[:7], IN_ORDER)
+    need = fwd_workspace_bytes(s0)
+    if need == 0:
+        raise UpipeError("upipe_fwd_workspace_bytes", EINVAL, "invalid shape")
+    ws = _workspace(need, dev) if ws is None else ws
+    flags = bytes(1 if h in fp8_heads else 0 for h in range(H))
+    st = Stats()
+    _check("upipe_attn_fwd_fp8", lib().upipe_attn_fwd_fp8(
+        _ptr(X, bf, "X"), _ptr(W_qkv, bf, "W_qkv"), _ptr(W_o, bf, "W_o"), *sh.args()[:7], flags,
+        _ptr(Y, bf, "Y"), _ptr(O_saved, bf, "O_saved"), _ptr(lse, f32, "lse"), _ptr(ws), ws.numel(),
+        _stream(stream), ctypes.byref(st)))
+    return Y, O_saved, lse, st.as_dict()
 
 
 def chunked_workspace_bytes(sh: Shape, n_chunks, backward) -> int:

@@ -45,17 +45,24 @@ struct FwdArgs {
   float* lse;
   float* o_acc;
   float* lse_acc;
+  const float* q_scale;  // FP8 scores: per query row
+  const float* k_scale;  // FP8 scores: per 128-key block, kv_ld / 128 per KV slot
   int* status;
 };
 
-template <int D>
+// F8: Q and K tiles hold E4M3 codes (one 128-byte swizzled row per query or
+// key at D = 128) and the scores come from kind::f8f6f4 MMAs; V, P and O stay
+// bf16.
+template <int D, bool F8 = false>
 struct FwdCfg {
-  static constexpr int TILE = BQ * D * 2;
+  static constexpr int TILE = BQ * D * 2;           // a bf16 tile (V)
+  static constexpr int QK_TILE = F8 ? BQ * D : TILE;  // a Q or K tile
+  static constexpr int QK_CHUNKS = QK_TILE / CH;      // 128-byte-wide column chunks
   static constexpr int QA_OFF = 0;
-  static constexpr int QB_OFF = TILE;
-  static constexpr int K_OFF = 2 * TILE;  // 2 stages
-  static constexpr int V_OFF = 4 * TILE;  // 2 stages
-  static constexpr int BAR_OFF = 6 * TILE;
+  static constexpr int QB_OFF = QK_TILE;
+  static constexpr int K_OFF = 2 * QK_TILE;            // 2 stages
+  static constexpr int V_OFF = 2 * QK_TILE + 2 * QK_TILE;  // 2 stages
+  static constexpr int BAR_OFF = V_OFF + 2 * TILE;
   static constexpr int SMEM = BAR_OFF + 256;
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns: S of tile t at t*128, O of tile t at 256 + t*D
@@ -63,11 +70,12 @@ struct FwdCfg {
   static __device__ __forceinline__ uint32_t t_o(int tile) { return 256u + static_cast<uint32_t>(tile) * D; }
 };
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdArgs a) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F8>;
+  static_assert(!F8 || D == 128, "FP8 scores need 128-byte Q and K rows");
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars + 0;
@@ -132,11 +140,11 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
-      mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::TILE);
+      mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::QK_TILE);
       for (int tile = 0; tile < (has_b ? 2 : 1); ++tile)
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(smem + (tile ? C::QB_OFF : C::QA_OFF) + c * CH, &tmQ, q_full, c * 64,
+        for (int c = 0; c < C::QK_CHUNKS; ++c)
+          tma_load_2d(smem + (tile ? C::QB_OFF : C::QA_OFF) + c * CH, &tmQ, q_full, c * (F8 ? 128 : 64),
                       slot * a.S + (tile ? qb1 : qb0) * BQ);
       // K of block j is last read by the scores of block j, one step before V of
       // block j is last read by P V: K runs one block ahead of V
@@ -144,10 +152,11 @@ __global__ void __launch_bounds__(384, 1)
         if (j < n_blocks) {
           const int s = j & 1;
           if (!mbar_wait(&k_empty[s], ((j >> 1) & 1) ^ 1, w, 20)) break;
-          mbar_arrive_expect_tx(&k_full[s], C::TILE);
+          mbar_arrive_expect_tx(&k_full[s], C::QK_TILE);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(smem + C::K_OFF + s * C::TILE + c * CH, &tmK, &k_full[s], c * 64, kvs * a.kv_ld + j * BKV);
+          for (int c = 0; c < C::QK_CHUNKS; ++c)
+            tma_load_2d(smem + C::K_OFF + s * C::QK_TILE + c * CH, &tmK, &k_full[s], c * (F8 ? 128 : 64),
+                        kvs * a.kv_ld + j * BKV);
         }
         if (j > 0) {
           const int jv = j - 1, s = jv & 1;
@@ -160,7 +169,7 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t ID_S = idesc_bf16(BQ, BKV, false, false);
+      constexpr uint32_t ID_S = F8 ? idesc_e4m3(BQ, BKV) : idesc_bf16(BQ, BKV, false, false);
       constexpr uint32_t ID_O = idesc_bf16(BQ, D, false, true);
       const uint32_t sQ[2] = {smem_u32(smem + C::QA_OFF), smem_u32(smem + C::QB_OFF)};
       bool ok = mbar_wait(q_full, 0, w, 21);
@@ -168,11 +177,15 @@ __global__ void __launch_bounds__(384, 1)
         const int s = j & 1;
         if (!mbar_wait(&k_full[s], (j >> 1) & 1, w, 22)) return false;
         tc_fence_after();
-        const uint64_t a0 = sdesc_kmajor(sQ[tile]), b0 = sdesc_kmajor(smem_u32(smem + C::K_OFF + s * C::TILE));
+        const uint64_t a0 = sdesc_kmajor(sQ[tile]), b0 = sdesc_kmajor(smem_u32(smem + C::K_OFF + s * C::QK_TILE));
+        // 32 bytes of each row per MMA: K = 16 bf16 or 32 E4M3 values
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
+        for (int k = 0; k < C::QK_TILE / BQ / 32; ++k) {
           const uint32_t off = (k >> 2) * CH + (k & 3) * 32;
-          mma_ss(tmem + C::t_s(tile), sdesc_advance(a0, off), sdesc_advance(b0, off), ID_S, k > 0);
+          if constexpr (F8)
+            mma_ss_f8(tmem + C::t_s(tile), sdesc_advance(a0, off), sdesc_advance(b0, off), ID_S, k > 0);
+          else
+            mma_ss(tmem + C::t_s(tile), sdesc_advance(a0, off), sdesc_advance(b0, off), ID_S, k > 0);
         }
         mma_commit(&s_full[tile]);
         return true;
@@ -225,12 +238,16 @@ __global__ void __launch_bounds__(384, 1)
         const int nkv = tile ? n_kv1 : n_kv0;
         const uint32_t t_s = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + C::t_s(tile);
         const uint32_t t_o = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + C::t_o(tile);
-        const float sl2 = a.scale_log2;
+        // scores times sl2 are the exponents in log2 units; FP8 scores carry the
+        // row's and the key block's scales as well
+        const float sl2_row = F8 ? a.scale_log2 * a.q_scale[static_cast<long long>(slot) * a.S + qi] : a.scale_log2;
+        const float* ksc = F8 ? a.k_scale + static_cast<long long>(kvs) * (a.kv_ld / BKV) : nullptr;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
           if (!mbar_wait_warp(&s_full[tile], j & 1, w, 25)) { ok = false; break; }
           tc_fence_after();
+          const float sl2 = F8 ? sl2_row * ksc[j] : sl2_row;
           const bool diag = has_diag && (j == nkv - 1);
           const int lim = diag ? qk - j * BKV : BKV;  // keys at column > lim are in the future
           // the whole row of S in one TMEM load: its maximum, then P from registers
@@ -385,17 +402,17 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t run_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
                     cudaStream_t st) {
-  auto kern = attn_fwd_kernel<D>;
+  auto kern = attn_fwd_kernel<D, F8>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D, F8>::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<args.n_qslots * args.q_pairs, 384, FwdCfg<D>::SMEM, st>>>(tq, tk, tv, args);
+  kern<<<args.n_qslots * args.q_pairs, 384, FwdCfg<D, F8>::SMEM, st>>>(tq, tk, tv, args);
   return cudaGetLastError();
 }
 
@@ -411,9 +428,15 @@ cudaError_t launch_attn_fwd(const AttnFwdDesc& d, int* status, cudaStream_t st) 
     return cudaErrorInvalidValue;
   for (int i = 0; i < d.n_qslots; ++i)
     if (d.kv_slot[i] >= d.n_kvslots) return cudaErrorInvalidValue;
+  if (d.fp8 && (d.D != 128 || !d.q_scale || !d.k_scale)) return cudaErrorInvalidValue;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16(&tq, d.Q, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tk, d.K, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
+  if (d.fp8) {
+    if (!make_tmap_u8(&tq, d.Q, d.D, (uint64_t)d.n_qslots * d.S, d.D, 128, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8(&tk, d.K, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 128, 128)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_tmap_bf16(&tq, d.Q, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&tk, d.K, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
+  }
   if (!make_tmap_bf16(&tv, d.V, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
   FwdArgs a;
   a.S = d.S;
@@ -424,6 +447,8 @@ cudaError_t launch_attn_fwd(const AttnFwdDesc& d, int* status, cudaStream_t st) 
   a.mode = d.mode;
   a.o_acc = d.o_acc;
   a.lse_acc = d.lse_acc;
+  a.q_scale = d.q_scale;
+  a.k_scale = d.k_scale;
   a.n_qslots = d.n_qslots;
   a.q_blocks = d.S / BQ;
   a.q_pairs = (a.q_blocks + 1) / 2;
@@ -435,7 +460,8 @@ cudaError_t launch_attn_fwd(const AttnFwdDesc& d, int* status, cudaStream_t st) 
   a.O = static_cast<uint16_t*>(d.O);
   a.lse = d.lse;
   a.status = status;
-  return d.D == 128 ? run_fwd<128>(tq, tk, tv, a, st) : run_fwd<64>(tq, tk, tv, a, st);
+  if (d.fp8) return run_fwd<128, true>(tq, tk, tv, a, st);
+  return d.D == 128 ? run_fwd<128, false>(tq, tk, tv, a, st) : run_fwd<64, false>(tq, tk, tv, a, st);
 }
 
 }  // namespace upipe

@@ -73,6 +73,12 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t o
                       box_outer);
 }
 
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
+                  uint32_t box_inner, uint32_t box_outer) {
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, inner, outer, row_stride_elems, box_inner,
+                      box_outer);
+}
+
 bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
                    uint32_t box_inner, uint32_t box_outer) {
   return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, inner, outer, row_stride_elems, box_inner,
@@ -414,15 +420,73 @@ struct Launcher {
     run(UPIPE_KERNEL_HEAD2SEQ, 0.0, b, [&] { return launch_dq_tiled_to_seq(p, st); });
     permute_bytes += static_cast<size_t>(b);
   }
+  void quant(const QuantDesc& p) {
+    const double b = static_cast<double>(p.n_slots) * p.S * p.D * (2 + 1) +
+                     4.0 * p.n_slots * (p.per_row ? p.S : p.S / 128);
+    run(UPIPE_KERNEL_SEQ2HEAD, 0.0, b, [&] { return launch_quant_e4m3(p, st); });
+    permute_bytes += static_cast<size_t>(b);
+  }
   void prep(const BwdPrepDesc& p) {
     const double b = static_cast<double>(p.n_slots) * p.S * (2.0 * 2 * p.D + 4.0 * p.D + 12.0);
     run(UPIPE_KERNEL_BWD_PREP, 0.0, b, [&] { return launch_bwd_prep(p, st); });
   }
 };
 
+// FP8 stage buffers inside the head-layout region of a stage: Q and K as E4M3
+// codes, V in bf16, the fp32 scales of Q rows and of 128-key blocks of K
+struct Fp8Stage {
+  uint8_t* q = nullptr;
+  uint8_t* k = nullptr;
+  uint16_t* v = nullptr;
+  float* qs = nullptr;
+  float* ks = nullptr;
+  size_t bytes = 0;
+};
+
+Fp8Stage fp8_stage_buffers(const Plan& p, uint8_t* base) {
+  const Shape& s = p.sh;
+  const size_t Sd = static_cast<size_t>(s.S) * s.d;
+  Fp8Stage f;
+  const size_t o_k = align256(s.U * Sd);
+  const size_t o_v = align256(o_k + p.n_kv_slots * Sd);
+  const size_t o_qs = align256(o_v + p.n_kv_slots * Sd * 2);
+  const size_t o_ks = align256(o_qs + static_cast<size_t>(s.U) * s.S * 4);
+  f.bytes = o_ks + static_cast<size_t>(p.n_kv_slots) * (s.S / 128) * 4;
+  if (base) {
+    f.q = base;
+    f.k = base + o_k;
+    f.v = reinterpret_cast<uint16_t*>(base + o_v);
+    f.qs = reinterpret_cast<float*>(base + o_qs);
+    f.ks = reinterpret_cast<float*>(base + o_ks);
+  }
+  return f;
+}
+
+// The exchange of an FP8 stage from the projected sequence buffer: Q rows and
+// K blocks encoded with their scales, V moved as bf16.
+void exchange_fp8(Launcher& L, const Plan& p, int i, const uint16_t* seq, const Fp8Stage& f) {
+  const Shape& s = p.sh;
+  const Stage& g = p.st[i];
+  const long long ld = static_cast<long long>(g.ncols()) * s.d;
+  const int nkv = static_cast<int>(g.kv_proj.size());
+  QuantDesc q;
+  q.src = seq; q.ld_src = ld; q.dst = f.q; q.scale = f.qs; q.S = s.S; q.D = s.d; q.n_slots = s.U; q.per_row = true;
+  for (int k = 0; k < s.U; ++k) q.src_head[k] = static_cast<uint16_t>(k);
+  L.quant(q);
+  QuantDesc kq;
+  kq.src = seq; kq.ld_src = ld; kq.dst = f.k; kq.scale = f.ks; kq.S = s.S; kq.D = s.d; kq.n_slots = p.n_kv_slots;
+  kq.per_row = false;
+  for (int k = 0; k < p.n_kv_slots; ++k) kq.src_head[k] = static_cast<uint16_t>(s.U + g.k_src[k]);
+  L.quant(kq);
+  Seq2HeadDesc x;
+  x.src = seq; x.ld_src = ld; x.dst = f.v; x.S = s.S; x.D = s.d; x.n_slots = p.n_kv_slots;
+  for (int k = 0; k < p.n_kv_slots; ++k) x.src_head[k] = static_cast<uint16_t>(s.U + nkv + g.k_src[k]);
+  L.s2h(x);
+}
+
 // QKV projection of one stage into the sequence buffer, then the exchange.
 void project_and_exchange(Launcher& L, const Plan& p, int i, const uint16_t* X, const uint16_t* W_qkv,
-                          uint8_t* ws, int set = 0) {
+                          uint8_t* ws, int set = 0, bool fp8 = false) {
   const Shape& s = p.sh;
   const Stage& g = p.st[i];
   uint16_t* seq = reinterpret_cast<uint16_t*>(ws + (set ? p.off_seq2 : p.off_seq));
@@ -435,6 +499,10 @@ void project_and_exchange(Launcher& L, const Plan& p, int i, const uint16_t* X, 
   head_blocks(gd.bmap_n, stage_wqkv_heads(s, g.q_heads, g.kv_proj), s.d);
   gd.out = seq; gd.ldo = static_cast<long long>(ncols) * s.d; gd.out_mode = kOutBf16;
   L.gemm(gd);
+  if (fp8) {
+    exchange_fp8(L, p, i, seq, fp8_stage_buffers(p, reinterpret_cast<uint8_t*>(qkvh)));
+    return;
+  }
   // exchange: Q slots, then (when this stage moves KV) K slots and V slots
   Seq2HeadDesc x;
   x.src = seq; x.ld_src = static_cast<long long>(ncols) * s.d;
@@ -510,7 +578,8 @@ namespace {
 
 int attn_fwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model, int H,
                    int G, int d_head, int U, int C, int sched, upipe_bf16* Y, upipe_bf16* O_saved, float* lse,
-                   void* ws, size_t ws_bytes, void* stream, upipe_stats* stats, bool allow_prefetch) {
+                   void* ws, size_t ws_bytes, void* stream, upipe_stats* stats, bool allow_prefetch,
+                   const uint8_t* fp8_heads = nullptr) {
   const Shape s{S, d_model, H, G, d_head, U, C, sched};
   if (check_shape(s) != UPIPE_OK) return check_shape(s);
   const Plan pmin = make_plan(s, false);
@@ -520,7 +589,7 @@ int attn_fwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
   // with room for a second stage-buffer set, stage i+1's projection and
   // exchange run on a second stream while stage i's attention runs
   const Plan ppf = pmin.n_stages > 1 ? make_plan(s, false, true) : pmin;
-  const bool pf = allow_prefetch && ppf.prefetch && ws_bytes >= ppf.total;
+  const bool pf = allow_prefetch && !fp8_heads && ppf.prefetch && ws_bytes >= ppf.total;
   const Plan& p = pf ? ppf : pmin;
   cudaStream_t st0 = static_cast<cudaStream_t>(stream), st1 = nullptr;
   cudaEvent_t ev[6] = {};  // fork, join, ready[2], free[2]
@@ -563,14 +632,19 @@ int attn_fwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
         cudaEventRecord(ev_ready[(i + 1) & 1], st1);
       }
       cudaStreamWaitEvent(st0, ev_ready[set], 0);
-    } else {
-      project_and_exchange(L, p, i, X, W_qkv, w);
     }
+    const bool f8 = fp8_heads && fp8_heads[g.q_heads[0]];
+    if (!pf) project_and_exchange(L, p, i, X, W_qkv, w, 0, f8);
     // (3) attention of the stage's heads
     AttnFwdDesc a;
     a.Q = qkvh;
     a.K = kvh + U * slot_elems;
     a.V = kvh + (U + p.n_kv_slots) * slot_elems;
+    if (f8) {
+      const Fp8Stage f = fp8_stage_buffers(p, reinterpret_cast<uint8_t*>(qkvh));
+      a.fp8 = true;
+      a.Q = f.q; a.K = f.k; a.V = f.v; a.q_scale = f.qs; a.k_scale = f.ks;
+    }
     a.O = oh;
     a.lse = lse;
     a.S = S; a.D = d; a.n_qslots = U; a.n_kvslots = p.n_kv_slots;
@@ -1571,6 +1645,72 @@ int upipe_attention_fwd(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf
     a.lse_row[k] = static_cast<uint16_t>(k);
   }
   return launch_attn_fwd(a, status, static_cast<cudaStream_t>(stream)) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
+}
+
+int upipe_quantize_e4m3(const upipe_bf16* src, int S, int n_heads, int d_head, long long src_row_stride,
+                        int per_row, uint8_t* dst, float* scales, void* stream) {
+  if (!src || !dst || !scales || !aligned16(src) || !aligned16(dst) || !aligned16(scales)) return UPIPE_EINVAL;
+  if (S <= 0 || S % 128 || n_heads <= 0 || src_row_stride < static_cast<long long>(n_heads) * d_head ||
+      src_row_stride % 8)
+    return UPIPE_EINVAL;
+  if (d_head != 64 && d_head != 128) return UPIPE_EUNSUPPORTED;
+  if (n_heads > kMaxSlots) return UPIPE_EUNSUPPORTED;
+  if (!device_supported()) return UPIPE_EUNSUPPORTED;
+  QuantDesc q;
+  q.src = src; q.ld_src = src_row_stride; q.dst = dst; q.scale = scales;
+  q.S = S; q.D = d_head; q.n_slots = n_heads; q.per_row = per_row != 0;
+  for (int k = 0; k < n_heads; ++k) q.src_head[k] = static_cast<uint16_t>(k);
+  return launch_quant_e4m3(q, static_cast<cudaStream_t>(stream)) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
+}
+
+int upipe_attention_fwd_fp8(const uint8_t* Q, const float* q_scale, const uint8_t* K, const float* k_scale,
+                            const upipe_bf16* V, int n_q, int n_kv, int S, int d_head, const int32_t* kv_of_q,
+                            upipe_bf16* O, float* lse, void* stream) {
+  const void* ptrs[] = {Q, q_scale, K, k_scale, V, O, lse};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return UPIPE_EINVAL;
+  if (!kv_of_q || n_q <= 0 || n_kv <= 0 || S <= 0 || S % 128) return UPIPE_EINVAL;
+  if (d_head != 128) return UPIPE_EUNSUPPORTED;
+  if (n_q > kMaxSlots) return UPIPE_EUNSUPPORTED;
+  for (int k = 0; k < n_q; ++k)
+    if (kv_of_q[k] < 0 || kv_of_q[k] >= n_kv) return UPIPE_EINVAL;
+  if (!device_supported()) return UPIPE_EUNSUPPORTED;
+  int* status = status_ptr();
+  if (!status) return UPIPE_ECUDA;
+  AttnFwdDesc a;
+  a.Q = Q; a.K = K; a.V = V; a.O = O; a.lse = lse;
+  a.fp8 = true; a.q_scale = q_scale; a.k_scale = k_scale;
+  a.S = S; a.D = d_head; a.n_qslots = n_q; a.n_kvslots = n_kv;
+  for (int k = 0; k < n_q; ++k) {
+    a.kv_slot[k] = static_cast<uint16_t>(kv_of_q[k]);
+    a.lse_row[k] = static_cast<uint16_t>(k);
+  }
+  return launch_attn_fwd(a, status, static_cast<cudaStream_t>(stream)) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
+}
+
+int upipe_attn_fwd_fp8(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model,
+                       int H, int G, int d_head, int U, int C, const uint8_t* fp8_heads, upipe_bf16* Y,
+                       upipe_bf16* O_saved, float* lse, void* ws, size_t ws_bytes, void* stream, upipe_stats* stats) {
+  const Shape s{S, d_model, H, G, d_head, U, C, UPIPE_SCHED_INORDER};
+  int rc = check_shape(s);
+  if (rc != UPIPE_OK) return rc;
+  if (!fp8_heads) return UPIPE_EINVAL;
+  const Plan p = make_plan(s, false);
+  bool any = false;
+  for (const Stage& g : p.st) {
+    const uint8_t f = fp8_heads[g.q_heads[0]] ? 1 : 0;
+    for (int h : g.q_heads)
+      if ((fp8_heads[h] ? 1 : 0) != f) return UPIPE_EINVAL;  // a stage runs in one precision
+    any = any || f;
+  }
+  if (any) {
+    if (d_head != 128) return UPIPE_EUNSUPPORTED;
+    // the FP8 buffers must fit where the stage's bf16 head-layout buffers go
+    const size_t region = static_cast<size_t>(U + 2 * p.n_kv_slots) * S * d_head * 2;
+    if (fp8_stage_buffers(p, nullptr).bytes > region) return UPIPE_EUNSUPPORTED;
+  }
+  return attn_fwd_issue(X, W_qkv, W_o, S, d_model, H, G, d_head, U, C, UPIPE_SCHED_INORDER, Y, O_saved, lse, ws,
+                        ws_bytes, stream, stats, false, any ? fp8_heads : nullptr);
 }
 
 int upipe_attention_bwd(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf16* V, const upipe_bf16* O,

@@ -61,6 +61,12 @@ struct AttnFwdDesc {
   int mode = kFwdPlain;
   float* o_acc = nullptr;    // [n_qslots][S][D] fp32 running output (merge modes)
   float* lse_acc = nullptr;  // [n_qslots][S] fp32 running log-sum-exp, log2 units
+  // FP8 scores (D = 128 only): Q and K hold E4M3 codes, one byte each; the
+  // score of (row r, key j) is their dot product times q_scale[slot][r] times
+  // k_scale[kv slot][j / 128] (k_scale rows are kv_ld / 128 long)
+  bool fp8 = false;
+  const float* q_scale = nullptr;
+  const float* k_scale = nullptr;
   uint16_t kv_slot[kMaxSlots];
   uint16_t lse_row[kMaxSlots];
 };
@@ -130,6 +136,18 @@ struct BwdPrepDesc {
   uint16_t lse_row[kMaxSlots];  // slot -> lse row
 };
 
+// Sequence layout (bf16) -> head layout in E4M3 codes, with fp32 scales
+// amax/448 (1 for an all-zero group): one per row (per_row) or one per 128
+// rows (per 128-key block).  S a multiple of 128, D 64 or 128.
+struct QuantDesc {
+  const uint16_t* src = nullptr; long long ld_src = 0;  // elements per token row
+  uint8_t* dst = nullptr;                               // [n_slots][S][D]
+  float* scale = nullptr;                               // [n_slots][S] or [n_slots][S/128]
+  int S = 0, D = 0, n_slots = 0;
+  bool per_row = true;
+  uint16_t src_head[kMaxSlots];
+};
+
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_gemm(const GemmDesc& g, int* status, cudaStream_t st);
 cudaError_t launch_attn_fwd(const AttnFwdDesc& a, int* status, cudaStream_t st);
@@ -138,10 +156,13 @@ cudaError_t launch_seq2head(const Seq2HeadDesc& p, cudaStream_t st);
 cudaError_t launch_head2seq(const Head2SeqDesc& p, cudaStream_t st);
 cudaError_t launch_bwd_prep(const BwdPrepDesc& p, cudaStream_t st);
 cudaError_t launch_dq_tiled_to_seq(const DqTiledDesc& p, cudaStream_t st);
+cudaError_t launch_quant_e4m3(const QuantDesc& p, cudaStream_t st);
 
 // Tensor maps (driver entry point resolved through the runtime).
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
                     uint32_t box_inner, uint32_t box_outer);
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
+                  uint32_t box_inner, uint32_t box_outer);
 bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
                    uint32_t box_inner, uint32_t box_outer);
 int num_sms();

@@ -239,6 +239,53 @@ int upipe_attention_fwd(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf
                         int d_head, const int32_t* kv_of_q, upipe_bf16* O, float* lse, void* stream);
 
 /*
+ * Lower-precision heads ("Untied Ulysses" summary page, paper.rainbus.top,
+ * section on weaknesses from an independent analysis: heads that can run in
+ * FP8 cut memory and communication further).  FP8 here is E4M3 (4 exponent
+ * bits, bias 7, 3 mantissa bits, largest finite 448), round to nearest even,
+ * saturating.
+ *
+ * upipe_quantize_e4m3: the exchange of such heads.  src: device bf16 in
+ * sequence layout, token t's head h at src[t * src_row_stride + h * d_head ..]
+ * (S a multiple of 128).  dst: device [n_heads][S][d_head] E4M3 codes (one
+ * byte each).  scales: device fp32, [n_heads][S] (per_row != 0: one scale per
+ * token and head) or [n_heads][S / 128] (one per block of 128 tokens).  Each
+ * scale is amax / 448 over its group in fp32 (IEEE division; 1 for an all-zero
+ * group) and each code is E4M3(x / scale) with x / scale an IEEE fp32
+ * division, so a value = code * scale.  d_head 64 or 128; n_heads <= 64.
+ */
+int upipe_quantize_e4m3(const upipe_bf16* src, int S, int n_heads, int d_head, long long src_row_stride,
+                        int per_row, uint8_t* dst, float* scales, void* stream);
+
+/*
+ * Causal GQA attention with FP8 scores: Q and K are E4M3 codes from
+ * upipe_quantize_e4m3 (Q per row, K per 128-key block); the score of query i
+ * and key j is (Q_i . K_j) * q_scale[i] * k_scale[j / 128] / sqrt(d_head),
+ * computed on the tensor cores' FP8 path; the softmax, P (bf16) and P V (bf16
+ * V) are as in upipe_attention_fwd, and so are O and lse.  d_head 128 only.
+ */
+int upipe_attention_fwd_fp8(const uint8_t* Q, const float* q_scale, const uint8_t* K, const float* k_scale,
+                            const upipe_bf16* V, int n_q, int n_kv, int S, int d_head, const int32_t* kv_of_q,
+                            upipe_bf16* O, float* lse, void* stream);
+
+/*
+ * The layer forward (in-order schedule) with the stages whose heads are
+ * flagged in fp8_heads (HOST array of H bytes, nonzero = FP8; every head of a
+ * stage must carry the same flag, else UPIPE_EINVAL) exchanging Q and K as
+ * E4M3 codes with their scales and attending with FP8 scores; V, O, Y and the
+ * other stages are as in upipe_attn_fwd, with the same workspace
+ * (upipe_fwd_workspace_bytes with the in-order schedule): an FP8 stage's
+ * buffers take (U + n_kv) S d_head bytes of codes plus 2 n_kv S d_head of V
+ * where the bf16 stage takes 2 (U + 2 n_kv) S d_head.  FP8 stages need
+ * d_head = 128 (UPIPE_EUNSUPPORTED otherwise).  O_saved and lse feed
+ * upipe_attn_bwd as usual; that backward recomputes in bf16, so its gradients
+ * are those of the bf16 layer at the FP8 forward's softmax statistics.
+ */
+int upipe_attn_fwd_fp8(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model,
+                       int H, int G, int d_head, int U, int C, const uint8_t* fp8_heads, upipe_bf16* Y,
+                       upipe_bf16* O_saved, float* lse, void* ws, size_t ws_bytes, void* stream, upipe_stats* stats);
+
+/*
  * Its backward pass.  dO: device bf16 [n_q][S][d_head]; O, lse from the forward.
  *   dQ  : device fp32 [n_q][S][d_head], output.
  *   dK, dV : device fp32 [n_kv][S][d_head], output (summed over the query
