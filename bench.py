@@ -261,7 +261,7 @@ def run_sweep(args):
     from synthetic import SHAPES
     dev = torch.device("cuda", 0)
     pk = peaks()
-    cases = []  # (name, shape, schedule, sequence chunks (0: none), offload store)
+    cases = []  # (name, shape, schedule, sequence chunks (0: none; -1: FP8 heads), offload store)
     us = SHAPES["llama3_8b_256k_usweep"]
     for U in (8, 16, 32):
         cases.append(("llama3_8b_256k_usweep", us.replace(U=U), 0, 0, None))
@@ -271,6 +271,8 @@ def run_sweep(args):
     # head stages on sequence chunks, K/V offloaded to page-locked host memory
     cases += [("llama3_8b_256k_chunked", us, 0, 8, "host"), ("llama3_8b_256k_chunked", us, 0, 16, "host"),
               ("llama3_8b_512k_chunked", gq, 0, 16, "host")]
+    # every head's scores in FP8 (forward), bf16 backward
+    cases += [("llama3_8b_32k_fp8", SHAPES["llama3_8b_32k"], 0, -1, None), ("llama3_8b_256k_fp8", us, 0, -1, None)]
     if args.sweep_only:
         cases = [c for c in cases if c[0] in args.sweep_only.split(",")]
     for name, sh, sched, n_chunks, where in cases:
@@ -283,7 +285,17 @@ def run_sweep(args):
         X, dY = randn(sh.S, sh.d_model), randn(sh.S, sh.d_model)
         Wqkv, Wo = randn(sh.d_model, sh.qkv_cols, std=w_std), randn(sh.H * sh.d_head, sh.d_model, std=w_std)
         store = None
-        if n_chunks:
+        if n_chunks < 0:
+            wsf = torch.empty(upipe.fwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
+            wsb = torch.empty(upipe.bwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
+            all_heads = set(range(sh.H))
+
+            def fwd(**kw):
+                return upipe.attn_fwd_fp8(X, Wqkv, Wo, s, all_heads, ws=wsf, **kw)
+
+            def bwd(O, lse, **kw):
+                return upipe.attn_bwd(X, Wqkv, Wo, O, lse, dY, s, ws=wsb, **kw)
+        elif n_chunks:
             wsf = torch.empty(upipe.chunked_workspace_bytes(s, n_chunks, False), dtype=torch.uint8, device=dev)
             wsb = torch.empty(upipe.chunked_workspace_bytes(s, n_chunks, True), dtype=torch.uint8, device=dev)
             store = torch.empty(upipe.chunked_store_bytes(s, n_chunks, True), dtype=torch.uint8)
@@ -333,7 +345,8 @@ def run_sweep(args):
             "permute_bytes_fwd": stf["permute_bytes"], "permute_bytes_bwd": stb["permute_bytes"],
             "persistent_bytes": stf["persistent_bytes"], "steps": args.sweep_steps, "clocks": clk,
             "workspace_fwd_bytes": wsf.numel(), "workspace_bwd_bytes": wsb.numel(),
-            "sequence_chunks": n_chunks, "offload_store": where, "offload_bytes": stb["offload_bytes"],
+            "sequence_chunks": max(n_chunks, 0), "fp8_heads": "all" if n_chunks < 0 else "none",
+            "offload_store": where, "offload_bytes": stb["offload_bytes"],
             "offload_copy_bytes": stf["offload_copy_bytes"] + stb["offload_copy_bytes"],
             "kernel_ms_per_step": {k: v[0] / args.sweep_steps for k, v in prof.items()}}), flush=True)
         del X, dY, Wqkv, Wo, wsf, wsb, Y, O, lse, dX, dWqkv, dWo, store, fwd, bwd
