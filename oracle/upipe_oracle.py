@@ -189,6 +189,25 @@ def attention_head_backward(q, k, v, P, o, do):
     return dq, dk, dv
 
 
+def attention_rows(q, k, v, do, rows):
+    """Forward and dQ of one head at the given query rows only (exact: row i
+    needs keys 0..i).  Returns (O [n, d], lse [n], dQ [n, d]) for those rows."""
+    d = q.shape[1]
+    O, L, dQ = [], [], []
+    for i in np.asarray(rows, dtype=np.int64):
+        s = k[:i + 1] @ q[i] / np.sqrt(d)
+        m = s.max()
+        e = np.exp(s - m)
+        p = e / e.sum()
+        o = p @ v[:i + 1]
+        dP = v[:i + 1] @ do[i]
+        dA = p * (dP - do[i] @ o)
+        O.append(o)
+        L.append(m + np.log(e.sum()))
+        dQ.append(dA @ k[:i + 1] / np.sqrt(d))
+    return np.array(O), np.array(L), np.array(dQ)
+
+
 # ---------------------------------------------------------------------------
 # the layer, all heads at once (the definition)
 # ---------------------------------------------------------------------------

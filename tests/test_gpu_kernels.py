@@ -148,3 +148,41 @@ def test_attention_first_row_copies_first_value(up):
     assert np.array_equal(bits_of(O)[0, 0], Vb[0, 0])
     s00 = float(bf16_bits_to_f64(Qb)[0, 0] @ bf16_bits_to_f64(Kb)[0, 0]) / np.sqrt(d)
     assert abs(f64_of(lse)[0, 0] - s00) < 1e-4
+
+
+def test_attention_core_full_size_32k(up):
+    """The attention launches of the Llama3-8B layer at S=32768 as the bench
+    times them (8 query slots, each with its own KV slot copy, d_head=128):
+    O, lse and dQ on sampled rows against the row-wise oracle, and two exact
+    identities of the whole backward: per KV slot, the rows of dV sum to the
+    sum of dO over its queries (rows of P sum to 1), and the rows of dK sum to
+    zero (each row of dS sums to dO.O - D = 0)."""
+    import torch
+    n, S, d = 8, 32768, 128
+    Qb = normal_bf16((n, S, d), 101)
+    Kb = normal_bf16((2, S, d), 102)
+    Vb = normal_bf16((2, S, d), 103)
+    dOb = normal_bf16((n, S, d), 104)
+    kv_head = [k // 4 for k in range(n)]
+    Kc = np.ascontiguousarray(Kb[kv_head])  # per-slot copies, as the in-order exchange makes them
+    Vc = np.ascontiguousarray(Vb[kv_head])
+    Q, K, V, dO = (to_dev(x) for x in (Qb, Kc, Vc, dOb))
+    O, lse = up.attention_fwd(Q, K, V, list(range(n)))
+    dQ, dK, dV = up.attention_bwd(Q, K, V, O, dO, lse, list(range(n)))
+    torch.cuda.synchronize()
+    up.sync_status()
+    rows = np.array([0, 1, 127, 128, 4095, 16384, 32767])
+    idx = torch.as_tensor(rows, device="cuda")
+    for h in (0, 5):
+        q, k, v, do = (bf16_bits_to_f64(x) for x in (Qb[h], Kb[kv_head[h]], Vb[kv_head[h]], dOb[h]))
+        o, l, dq = orc.attention_rows(q, k, v, do, rows)
+        assert rel(f64_of(O[h][idx]), o) < 1e-2
+        assert np.abs(f64_of(lse[h][idx]) - l).max() < 2e-3
+        assert rel(f64_of(dQ[h][idx]), dq) < 1e-2
+    dVs = dV.double().sum(dim=1).cpu().numpy()
+    dKs = dK.double().sum(dim=1).cpu().numpy()
+    dKn = dK.double().norm(dim=2).sum(dim=1).cpu().numpy()
+    do_sum = bf16_bits_to_f64(dOb).sum(axis=1)
+    for k in range(n):
+        assert rel(dVs[k], do_sum[k]) < 1e-2
+        assert np.linalg.norm(dKs[k]) < 1e-2 * dKn[k]

@@ -215,3 +215,17 @@ def test_tiny_workload_bf16_inputs_staged_equals_plain():
     for order in (orc.IN_ORDER, orc.GQA_OUT_OF_ORDER):
         Ys = orc.staged_forward(X, W_qkv, W_o, sh.H, sh.G, sh.d_head, sh.U, sh.C, order)[0]
         assert np.linalg.norm(Ys - Y) <= 1e-12 * np.linalg.norm(Y)
+
+
+def test_attention_rows_match_the_whole_head():
+    """The row-wise forward and dQ (used to check full-size launches on sampled
+    rows) against the whole-head oracle."""
+    rng = np.random.default_rng(9)
+    S, d = 48, 8
+    q, k, v, do = (rng.standard_normal((S, d)) for _ in range(4))
+    o, l, P = orc.attention_head_forward(q, k, v)
+    dq, _, _ = orc.attention_head_backward(q, k, v, P, o, do)
+    rows = [0, 1, 17, 47]
+    ro, rl, rdq = orc.attention_rows(q, k, v, do, rows)
+    assert np.abs(ro - o[rows]).max() < 1e-13 and np.abs(rl - l[rows]).max() < 1e-13
+    assert np.abs(rdq - dq[rows]).max() < 1e-13
