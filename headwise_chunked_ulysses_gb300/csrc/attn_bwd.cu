@@ -77,11 +77,12 @@ struct BwdCfg {
 // The (query slot, query block) pairs a CTA visits, in order: the query
 // blocks at or after its KV block (query block b sits at KV block
 // b + q_off_blocks).
+template <bool GEN>
 struct ItemCursor {
   int qs = -1, qb = 0, qb_first = 0, q_blocks = 0;
   bool primed = false;
   __device__ bool next(const BwdArgs& a, int kvs) {
-    if (primed) { primed = false; return true; }
+    if (GEN && primed) { primed = false; return true; }
     if (qs >= 0 && ++qb < q_blocks) return true;
     for (++qs; qs < a.n_qslots; ++qs)
       if (a.kv_slot[qs] == kvs) { qb = qb_first; return true; }
@@ -90,7 +91,7 @@ struct ItemCursor {
   // position on item k (0-based) of this KV slot; next() then returns it first
   __device__ void seek(const BwdArgs& a, int kvs, int k) {
     const int per_slot = q_blocks - qb_first;
-    if (k <= 0 || per_slot <= 0) return;
+    if (!GEN || k <= 0 || per_slot <= 0) return;
     int skip = k / per_slot;
     for (qs = 0; qs < a.n_qslots; ++qs)
       if (a.kv_slot[qs] == kvs && skip-- == 0) break;
@@ -99,7 +100,9 @@ struct ItemCursor {
   }
 };
 
-template <int D>
+// GEN: key offsets, key ranges and split KV blocks (chunk pairs); without it
+// the launch is the plain causal case and those paths compile away.
+template <int D, bool GEN>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -131,19 +134,23 @@ __global__ void __launch_bounds__(512, 1)
   // (most work) first, so the CTAs running at one time share few slots'
   // query-side data
   const int grp_slots = a.grp_slots;
+  const int q_split = GEN ? a.q_split : 1;
+  const int q_off_blocks = GEN ? a.q_off_blocks : 0;
+  const int kv_blocks = GEN ? a.kv_blocks : a.q_blocks;
+  const int kv_ld = GEN ? a.kv_ld : a.S;
   // (the q_split CTAs of one KV block are adjacent in launch order)
-  const int part = static_cast<int>(blockIdx.x) % a.q_split;
-  const int cta = static_cast<int>(blockIdx.x) / a.q_split;
-  const int per_grp = grp_slots * a.kv_blocks;
+  const int part = GEN ? static_cast<int>(blockIdx.x) % q_split : 0;
+  const int cta = GEN ? static_cast<int>(blockIdx.x) / q_split : static_cast<int>(blockIdx.x);
+  const int per_grp = grp_slots * kv_blocks;
   const int grp = cta / per_grp, rem = cta % per_grp;
   const int kvb = rem / grp_slots;
   const int kvs = grp * grp_slots + rem % grp_slots;
   int n_q = 0;
   for (int i = 0; i < a.n_qslots; ++i) n_q += (a.kv_slot[i] == kvs);
-  const int qb_first = max(0, kvb - a.q_off_blocks);
+  const int qb_first = GEN ? max(0, kvb - q_off_blocks) : kvb;
   const int n_all = n_q * max(0, a.q_blocks - qb_first);
-  const int item0 = static_cast<int>(static_cast<long long>(n_all) * part / a.q_split);
-  const int n_items = static_cast<int>(static_cast<long long>(n_all) * (part + 1) / a.q_split) - item0;
+  const int item0 = GEN ? static_cast<int>(static_cast<long long>(n_all) * part / q_split) : 0;
+  const int n_items = GEN ? static_cast<int>(static_cast<long long>(n_all) * (part + 1) / q_split) - item0 : n_all;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -178,14 +185,14 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmdO);
-      const int kv_row = kvs * a.kv_ld + kvb * BKV;
+      const int kv_row = kvs * kv_ld + kvb * BKV;
       mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         tma_load_2d(smem + C::K_OFF + c * CH, &tmK, kv_full, c * 64, kv_row);
         tma_load_2d(smem + C::V_OFF + c * CH, &tmV, kv_full, c * 64, kv_row);
       }
-      ItemCursor cur;
+      ItemCursor<GEN> cur;
       cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
       cur.seek(a, kvs, item0);
@@ -287,7 +294,7 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t sDS = smem_u32(smem + C::DS_TILE_OFF);
       const float sl2 = a.scale_log2;
       const uint64_t sl2x2 = f2(sl2, sl2);
-      ItemCursor cur;
+      ItemCursor<GEN> cur;
       cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
       cur.seek(a, kvs, item0);
@@ -295,7 +302,7 @@ __global__ void __launch_bounds__(512, 1)
       int i = 0;
       for (; i < n_items && cur.next(a, kvs); ++i) {
         const int st = i & 1;
-        const bool diag = (cur.qb + a.q_off_blocks == kvb);
+        const bool diag = (cur.qb + q_off_blocks == kvb);
         if (!mbar_wait_warp(s_full, i & 1, w, 47)) { ok = false; break; }
         if (!mbar_wait_warp(&qdo_full[st], (i >> 1) & 1, w, 48)) { ok = false; break; }
         tc_fence_after();
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(512, 1)
       // dK, dV epilogue: this thread's half of the d columns of KV row `row`
       if (ok && mbar_wait_warp(kv_done, 0, w, 52)) {
         tc_fence_after();
-        const long long base = (static_cast<long long>(kvs) * a.kv_ld + kv_idx) * D + half * (D / 2);
+        const long long base = (static_cast<long long>(kvs) * kv_ld + kv_idx) * D + half * (D / 2);
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
           float* dst = (which == 0 ? a.dV : a.dK) + base;
@@ -379,7 +386,7 @@ __global__ void __launch_bounds__(512, 1)
             for (int e = 0; e < 8; ++e) {
               float4 x = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
                                      __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
-              if (a.q_split > 1) {  // other CTAs add to the same rows
+              if (GEN && q_split > 1) {  // other CTAs add to the same rows
                 red_add_v4(dst + c * 32 + 4 * e, x.x, x.y, x.z, x.w);
                 continue;
               }
@@ -399,7 +406,7 @@ __global__ void __launch_bounds__(512, 1)
       // warps' path
       const int row = (warp & 3) * 32 + lane;
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      ItemCursor cur;
+      ItemCursor<GEN> cur;
       cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
       cur.seek(a, kvs, item0);
@@ -427,11 +434,11 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
     }
-  } else if (aligned && n_items == 0 && !a.accumulate_kv && a.q_split == 1 && warp >= 4 && warp < 12) {
+  } else if (aligned && n_items == 0 && !a.accumulate_kv && q_split == 1 && warp >= 4 && warp < 12) {
     // a KV slot no query head uses in this launch: its gradient is zero
     const int row = (warp & 3) * 32 + lane;
     const int half = (warp - 4) >> 2;
-    const long long base = (static_cast<long long>(kvs) * a.kv_ld + kvb * BKV + row) * D + half * (D / 2);
+    const long long base = (static_cast<long long>(kvs) * kv_ld + kvb * BKV + row) * D + half * (D / 2);
     for (int c = 0; c < D / 2; c += 4) {
       *reinterpret_cast<float4*>(a.dK + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
       *reinterpret_cast<float4*>(a.dV + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -504,9 +511,9 @@ __global__ void __launch_bounds__(256) dq_tiled_to_seq_kernel(const DqTiledDesc 
   }
 }
 
-template <int D>
+template <int D, bool GEN>
 cudaError_t run_bwd(const CUtensorMap* tm, const BwdArgs& args, cudaStream_t st) {
-  auto kern = attn_bwd_kernel<D>;
+  auto kern = attn_bwd_kernel<D, GEN>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::SMEM);
@@ -576,7 +583,9 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) 
   a.dK = d.dK;
   a.dV = d.dV;
   a.status = status;
-  return d.D == 128 ? run_bwd<128>(tm, a, st) : run_bwd<64>(tm, a, st);
+  const bool gen = d.q_off != 0 || kv_len != d.S || kv_ld != d.S || d.q_split > 1;
+  if (gen) return d.D == 128 ? run_bwd<128, true>(tm, a, st) : run_bwd<64, true>(tm, a, st);
+  return d.D == 128 ? run_bwd<128, false>(tm, a, st) : run_bwd<64, false>(tm, a, st);
 }
 
 }  // namespace upipe

@@ -70,7 +70,9 @@ struct FwdCfg {
   static __device__ __forceinline__ uint32_t t_o(int tile) { return 256u + static_cast<uint32_t>(tile) * D; }
 };
 
-template <int D, bool F8>
+// GEN: key offsets and ranges, and the merging epilogues (chunk pairs);
+// without it the launch is the plain causal case and those paths compile away.
+template <int D, bool F8, bool GEN>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdArgs a) {
@@ -106,8 +108,11 @@ __global__ void __launch_bounds__(384, 1)
   const bool has_b = qb1 < a.q_blocks;
   // query block b sits at KV block b + q_off_blocks: it sees the KV blocks up
   // to that one (the diagonal, masked) or all of them when it lies beyond
-  const int n_kv0 = min(a.kv_blocks, qb0 + a.q_off_blocks + 1);
-  const int n_kv1 = has_b ? min(a.kv_blocks, qb1 + a.q_off_blocks + 1) : 0;
+  const int q_off_blocks = GEN ? a.q_off_blocks : 0;
+  const int kv_blocks = GEN ? a.kv_blocks : a.q_blocks;
+  const int kv_ld = GEN ? a.kv_ld : a.S;
+  const int n_kv0 = GEN ? min(kv_blocks, qb0 + q_off_blocks + 1) : qb0 + 1;
+  const int n_kv1 = has_b ? (GEN ? min(kv_blocks, qb1 + q_off_blocks + 1) : qb1 + 1) : 0;
   const int n_blocks = has_b ? n_kv1 : n_kv0;
 
   if (threadIdx.x == 0) {
@@ -156,7 +161,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int c = 0; c < C::QK_CHUNKS; ++c)
             tma_load_2d(smem + C::K_OFF + s * C::QK_TILE + c * CH, &tmK, &k_full[s], c * (F8 ? 128 : 64),
-                        kvs * a.kv_ld + j * BKV);
+                        kvs * kv_ld + j * BKV);
         }
         if (j > 0) {
           const int jv = j - 1, s = jv & 1;
@@ -164,7 +169,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&v_full[s], C::TILE);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(smem + C::V_OFF + s * C::TILE + c * CH, &tmV, &v_full[s], c * 64, kvs * a.kv_ld + jv * BKV);
+            tma_load_2d(smem + C::V_OFF + s * C::TILE + c * CH, &tmV, &v_full[s], c * 64, kvs * kv_ld + jv * BKV);
         }
       }
     } else if (warp == 1 && lane == 0) {
@@ -233,15 +238,15 @@ __global__ void __launch_bounds__(384, 1)
         const int row = q4 * 32 + lane;
         const int qb = tile ? qb1 : qb0;
         const int qi = qb * BQ + row;                     // row of the query slot
-        const int qk = qi + a.q_off_blocks * BQ;          // its position among the keys
-        const bool has_diag = qb + a.q_off_blocks < a.kv_blocks;
+        const int qk = qi + q_off_blocks * BQ;            // its position among the keys
+        const bool has_diag = !GEN || qb + q_off_blocks < kv_blocks;
         const int nkv = tile ? n_kv1 : n_kv0;
         const uint32_t t_s = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + C::t_s(tile);
         const uint32_t t_o = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + C::t_o(tile);
         // scores times sl2 are the exponents in log2 units; FP8 scores carry the
         // row's and the key block's scales as well
         const float sl2_row = F8 ? a.scale_log2 * a.q_scale[static_cast<long long>(slot) * a.S + qi] : a.scale_log2;
-        const float* ksc = F8 ? a.k_scale + static_cast<long long>(kvs) * (a.kv_ld / BKV) : nullptr;
+        const float* ksc = F8 ? a.k_scale + static_cast<long long>(kvs) * (kv_ld / BKV) : nullptr;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
@@ -326,8 +331,8 @@ __global__ void __launch_bounds__(384, 1)
           const long long orow_idx = static_cast<long long>(slot) * a.S + qi;
           uint16_t* orow = a.O + orow_idx * D;
           const float lse2_part = m_run + __log2f(l_run);  // this launch's keys, log2 units
-          float* lrow = a.lse + static_cast<long long>(a.lse_row[slot]) * a.lse_ld + qi;
-          if (a.mode == kFwdPlain) {
+          float* lrow = a.lse + static_cast<long long>(a.lse_row[slot]) * (GEN ? a.lse_ld : a.S) + qi;
+          if (!GEN || a.mode == kFwdPlain) {
             const float inv = 1.f / l_run;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
@@ -402,10 +407,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool F8>
+template <int D, bool F8, bool GEN>
 cudaError_t run_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
                     cudaStream_t st) {
-  auto kern = attn_fwd_kernel<D, F8>;
+  auto kern = attn_fwd_kernel<D, F8, GEN>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D, F8>::SMEM);
@@ -460,8 +465,10 @@ cudaError_t launch_attn_fwd(const AttnFwdDesc& d, int* status, cudaStream_t st) 
   a.O = static_cast<uint16_t*>(d.O);
   a.lse = d.lse;
   a.status = status;
-  if (d.fp8) return run_fwd<128, true>(tq, tk, tv, a, st);
-  return d.D == 128 ? run_fwd<128, false>(tq, tk, tv, a, st) : run_fwd<64, false>(tq, tk, tv, a, st);
+  const bool gen = d.q_off != 0 || kv_len != d.S || kv_ld != d.S || a.lse_ld != d.S || d.mode != kFwdPlain;
+  if (d.fp8) return gen ? cudaErrorInvalidValue : run_fwd<128, true, false>(tq, tk, tv, a, st);
+  if (gen) return d.D == 128 ? run_fwd<128, false, true>(tq, tk, tv, a, st) : run_fwd<64, false, true>(tq, tk, tv, a, st);
+  return d.D == 128 ? run_fwd<128, false, false>(tq, tk, tv, a, st) : run_fwd<64, false, false>(tq, tk, tv, a, st);
 }
 
 }  // namespace upipe
