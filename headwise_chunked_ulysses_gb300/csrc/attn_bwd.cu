@@ -106,7 +106,7 @@ template <int D, bool GEN>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                    const __grid_constant__ BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* s_full = bars + 5;
   uint64_t* dp_full = bars + 6;
   uint64_t* p_ready = bars + 7;
+  uint64_t* dq_staged = bars + 8;  // dQ_i has left the dS tile (TMA reduce mode)
   uint64_t* ds_ready = bars + 9;
   uint64_t* ds_consumed = bars + 10;
   uint64_t* dq_full = bars + 11;
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(ds_consumed, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_drained, 128);
+    mbar_init(dq_staged, 128);
     mbar_init(kv_done, 1);
     *abort_flag = aligned ? 0 : 1;
     if (!aligned && a.status) atomicCAS(a.status, 0, kDevBadSmem);
@@ -355,8 +357,12 @@ __global__ void __launch_bounds__(512, 1)
             pk[(q0 >> 1) + 1] = pack_bf16(f2_lo(db), f2_hi(db));
           }
         }
-        // the dS^T buffer is free once the previous step's dK and dQ MMAs are done
-        if (i > 0 && !mbar_wait_warp(ds_consumed, (i - 1) & 1, w, 49)) { ok = false; break; }
+        // the dS^T tile is free once the previous step's dQ MMA has read it (and,
+        // when dQ leaves through the TMA engine, once dQ's staging in it is read)
+        if (i > 0 && !mbar_wait_warp(a.dq_tiled == 2 ? dq_staged : ds_consumed, (i - 1) & 1, w, 49)) {
+          ok = false;
+          break;
+        }
         // dS^T as bf16 pairs into the other 32 of this half's S^T columns (the A
         // operand of dK), and into shared memory (the A operand of dQ)
         tmem_st32(tmem + lane_off + C::T_S + half * 64 + 32, pk);
@@ -410,27 +416,82 @@ __global__ void __launch_bounds__(512, 1)
       cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
       cur.seek(a, kvs, item0);
-      for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
-        if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
-        tc_fence_after();
-        const long long qrow = static_cast<long long>(cur.qs) * a.S + cur.qb * BQ + row;
-        // address of the 4 columns starting at column 4*g of query row qrow
-        auto col4 = [&](int g) -> float* {
-          return a.dq_tiled ? a.dQacc + ((qrow >> 5) * (D / 4) + g) * 128 + (qrow & 31) * 4
-                            : a.dQacc + qrow * D + 4 * g;
-        };
+      if (a.dq_tiled == 2) {
+        // row-major fp32 dQ through the TMA engine: each warp stages its 32
+        // rows in 32-column chunks (32 x 32 fp32, 128-byte swizzle) in its
+        // 8 KB quarter of the dS tile, two buffers, and issues element-wise
+        // reduce-adds, so the reductions leave the SM without load/store
+        // instructions; the tile is handed back to the softmax warps once
+        // the engine has read the last chunk
+        tma_prefetch_map(&tmDQ);
+        const uint32_t stage = smem_u32(smem + C::DS_TILE_OFF) + (warp & 3) * 8192;
+        int nb = 0;
+        for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
+          if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
+          tc_fence_after();
+          const int y0 = cur.qs * a.S + cur.qb * BQ + (warp & 3) * 32;
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t v[64];
+            tmem_ld64(tmem + lane_off + C::T_DP + c * 64, v);
+            if (c == D / 64 - 1) {
+              tc_fence_before();
+              mbar_arrive(dq_drained);
+            }
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[64];
-          tmem_ld64(tmem + lane_off + C::T_DP + c * 64, v);
-          if (c == D / 64 - 1) {
-            tc_fence_before();
-            mbar_arrive(dq_drained);
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t buf = stage + (nb & 1) * 4096;
+              if (nb >= 2) {  // the chunk sent two chunks ago has left this buffer
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+              }
+#pragma unroll
+              for (int p = 0; p < 8; ++p)
+                st_shared_v4(buf + lane * 128 + ((p ^ (lane & 7)) << 4),
+                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p]) * a.scale),
+                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 1]) * a.scale),
+                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 2]) * a.scale),
+                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 3]) * a.scale));
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_reduce_add_2d(&tmDQ, buf, c * 64 + h * 32, y0);
+                bulk_commit();
+              }
+              ++nb;
+            }
           }
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          mbar_arrive(dq_staged);
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+      } else {
+        // vector reductions from the registers, tiled or row-major
+        for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
+          if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
+          tc_fence_after();
+          const long long qrow = static_cast<long long>(cur.qs) * a.S + cur.qb * BQ + row;
+          // address of the 4 columns starting at column 4*g of query row qrow
+          auto col4 = [&](int g) -> float* {
+            return a.dq_tiled ? a.dQacc + ((qrow >> 5) * (D / 4) + g) * 128 + (qrow & 31) * 4
+                              : a.dQacc + qrow * D + 4 * g;
+          };
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            red_add_v4(col4(c * 16 + e), __uint_as_float(v[4 * e]) * a.scale, __uint_as_float(v[4 * e + 1]) * a.scale,
-                       __uint_as_float(v[4 * e + 2]) * a.scale, __uint_as_float(v[4 * e + 3]) * a.scale);
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t v[64];
+            tmem_ld64(tmem + lane_off + C::T_DP + c * 64, v);
+            if (c == D / 64 - 1) {
+              tc_fence_before();
+              mbar_arrive(dq_drained);
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              red_add_v4(col4(c * 16 + e), __uint_as_float(v[4 * e]) * a.scale,
+                         __uint_as_float(v[4 * e + 1]) * a.scale, __uint_as_float(v[4 * e + 2]) * a.scale,
+                         __uint_as_float(v[4 * e + 3]) * a.scale);
+          }
         }
       }
     }
@@ -520,7 +581,8 @@ cudaError_t run_bwd(const CUtensorMap* tm, const BwdArgs& args, cudaStream_t st)
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<args.n_kvslots * args.kv_blocks * args.q_split, 512, BwdCfg<D>::SMEM, st>>>(tm[0], tm[1], tm[2], tm[3], args);
+  kern<<<args.n_kvslots * args.kv_blocks * args.q_split, 512, BwdCfg<D>::SMEM, st>>>(tm[0], tm[1], tm[2], tm[3], tm[4],
+                                                                                      args);
   return cudaGetLastError();
 }
 
@@ -552,11 +614,18 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) 
   if (d.q_split < 1 || d.q_split > 16) return cudaErrorInvalidValue;
   for (int i = 0; i < d.n_qslots; ++i)
     if (d.kv_slot[i] >= d.n_kvslots) return cudaErrorInvalidValue;
-  CUtensorMap tm[4];
+  if (d.dq_tiled < 0 || d.dq_tiled > 2) return cudaErrorInvalidValue;
+  CUtensorMap tm[5];
   if (!make_tmap_bf16(&tm[0], d.Q, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tm[1], d.K, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tm[2], d.V, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tm[3], d.dO, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
+  // dQ accumulator as fp32 rows for the TMA reduce mode (otherwise unused)
+  if (d.dq_tiled == 2) {
+    if (!make_tmap_f32(&tm[4], d.dQacc, d.D, (uint64_t)d.n_qslots * d.S, d.D, 32, 32)) return cudaErrorInvalidValue;
+  } else {
+    tm[4] = tm[3];
+  }
   BwdArgs a;
   a.S = d.S;
   a.kv_ld = kv_ld;

@@ -791,7 +791,7 @@ int attn_bwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
     ab.dK = dacc + U * slot_elems;
     ab.dV = dacc + (U + p.n_kv_slots) * slot_elems;
     ab.accumulate_kv = (ooo && i > 0) ? 1 : 0;
-    ab.dq_tiled = 1;
+    ab.dq_tiled = 2;
     ab.S = S; ab.D = d; ab.n_qslots = U; ab.n_kvslots = p.n_kv_slots;
     for (int k = 0; k < U; ++k) ab.kv_slot[k] = static_cast<uint16_t>(g.kv_of_q[k]);
     L.bwd(ab);
@@ -801,10 +801,15 @@ int attn_bwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
     for (int part = 0; part < 2; ++part)
       for (int m = 0; m < nkv; ++m) wheads.push_back((part == 0 ? H : H + G) + g.kv_proj[m]);
     const long long ld_dseq = static_cast<long long>(wheads.size()) * d;
-    DqTiledDesc qb;
-    qb.src = dacc; qb.dst = seq; qb.ld_dst = ld_dseq; qb.S = S; qb.D = d; qb.n_slots = U;
-    for (int k = 0; k < U; ++k) qb.dst_head[k] = static_cast<uint16_t>(k);
-    L.dq2s(qb);
+    Head2SeqDesc qb;  // row-major fp32 dQ -> bf16
+    qb.src = dacc; qb.src_f32 = true;
+    qb.dst = seq; qb.ld_dst = ld_dseq; qb.S = S; qb.D = d; qb.n_heads = U;
+    for (int k = 0; k <= U; ++k) qb.first[k] = static_cast<uint16_t>(k);
+    for (int k = 0; k < U; ++k) {
+      qb.dst_head[k] = static_cast<uint16_t>(k);
+      qb.src_slot[k] = static_cast<uint16_t>(k);
+    }
+    L.h2s(qb);
     if (nkv > 0) {
       Head2SeqDesc hb;
       hb.src = dacc; hb.src_f32 = true;
@@ -1303,7 +1308,7 @@ int attn_bwd_chunked_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const u
       const int n_out = U + (final_here ? 2 * nkv : 0);
       const long long ld_dseq = static_cast<long long>(n_out) * d;
       AttnBwdDesc ab;
-      ab.Q = qh; ab.dO = doh; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dq; ab.dq_tiled = 1;
+      ab.Q = qh; ab.dO = doh; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dq; ab.dq_tiled = 2;
       ab.S = Sc; ab.D = d; ab.n_qslots = U; ab.n_kvslots = nkv;
       ab.kv_len = Sc; ab.kv_ld = Sc;
       ab.accumulate_kv = acc ? 1 : 0;
@@ -1347,10 +1352,15 @@ int attn_bwd_chunked_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const u
           cst.copy(dkv_at(j, 1, g0), dkw + nkv * chunk_elems, nkv * chunk_elems * 4);
         }
       }
-      DqTiledDesc qb;
-      qb.src = dq; qb.dst = seq; qb.ld_dst = ld_dseq; qb.S = Sc; qb.D = d; qb.n_slots = U;
-      for (int k = 0; k < U; ++k) qb.dst_head[k] = static_cast<uint16_t>(k);
-      L.dq2s(qb);
+      Head2SeqDesc qb;  // row-major fp32 dQ -> bf16
+      qb.src = dq; qb.src_f32 = true;
+      qb.dst = seq; qb.ld_dst = ld_dseq; qb.S = Sc; qb.D = d; qb.n_heads = U;
+      for (int k = 0; k <= U; ++k) qb.first[k] = static_cast<uint16_t>(k);
+      for (int k = 0; k < U; ++k) {
+        qb.dst_head[k] = static_cast<uint16_t>(k);
+        qb.src_slot[k] = static_cast<uint16_t>(k);
+      }
+      L.h2s(qb);
       // dX rows of the chunk (+)= dQKV W_qkv[:, heads]^T ; dW_qkv[:, heads] += X_chunk^T dQKV
       std::vector<int> wheads(g.q_heads.begin(), g.q_heads.end());
       if (final_here)

@@ -81,7 +81,8 @@ struct AttnBwdDesc {
   float* dQacc = nullptr;    // fp32 per query slot, pre-zeroed, atomically accumulated
   // dQacc layout: 0 = [slot][S][D] row-major; 1 = tiled [slot][S/32][D/4][32][4]
   // (32 consecutive rows of one 4-wide column group contiguous, so one warp's
-  // vector reduction covers a single 512-byte run)
+  // vector reduction covers a single 512-byte run); 2 = row-major, added by
+  // TMA reduce-adds of 32 x 32 chunks staged in shared memory
   int dq_tiled = 0;
   float* dK = nullptr;       // [n_kvslots][kv_ld][D] fp32
   float* dV = nullptr;       // [n_kvslots][kv_ld][D] fp32
