@@ -415,11 +415,6 @@ struct Launcher {
     run(UPIPE_KERNEL_HEAD2SEQ, 0.0, b, [&] { return launch_head2seq(p, st); });
     permute_bytes += static_cast<size_t>(b);
   }
-  void dq2s(const DqTiledDesc& p) {
-    const double b = static_cast<double>(p.n_slots) * p.S * p.D * (4 + 2);
-    run(UPIPE_KERNEL_HEAD2SEQ, 0.0, b, [&] { return launch_dq_tiled_to_seq(p, st); });
-    permute_bytes += static_cast<size_t>(b);
-  }
   void quant(const QuantDesc& p) {
     const double b = static_cast<double>(p.n_slots) * p.S * p.D * (2 + 1) +
                      4.0 * p.n_slots * (p.per_row ? p.S : p.S / 128);
