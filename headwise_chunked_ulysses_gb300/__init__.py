@@ -29,7 +29,7 @@ EXPORTS = (
     "upipe_sync_status", "upipe_status_str", "upipe_version", "upipe_profile_enable", "upipe_profile_read",
     "upipe_graphs_enable", "upipe_chunked_workspace_bytes", "upipe_chunked_store_bytes",
     "upipe_attn_fwd_chunked", "upipe_attn_bwd_chunked",
-    "upipe_quantize_e4m3", "upipe_attention_fwd_fp8", "upipe_attn_fwd_fp8",
+    "upipe_quantize_e4m3", "upipe_attention_fwd_fp8", "upipe_attn_fwd_fp8", "upipe_choose_chunks",
 )
 
 
@@ -88,6 +88,7 @@ def _sig(lib):
         "upipe_attention_fwd_fp8": (I, [P, P, P, P, P, I, I, I, I, i32p, P, P, P]),
         "upipe_attn_fwd_fp8": (I, [P, P, P] + [I] * 7 + [ctypes.c_char_p, P, P, P, P, Z, P, P]),
         "upipe_chunked_workspace_bytes": (Z, [I] * 9),
+        "upipe_choose_chunks": (I, [I] * 7 + [Z]),
         "upipe_chunked_store_bytes": (Z, [I] * 9),
         "upipe_attn_fwd_chunked": (I, [P, P, P] + [I] * 8 + [P, P, P, P, Z, P, Z, P, P]),
         "upipe_attn_bwd_chunked": (I, [P, P, P] + [I] * 8 + [P, P, P, P, P, P, P, Z, P, Z, P, P]),
@@ -291,6 +292,12 @@ def attn_fwd_fp8(X, W_qkv, W_o, sh: Shape, fp8_heads, Y=None, O_saved=None, lse=
 
 def chunked_workspace_bytes(sh: Shape, n_chunks, backward) -> int:
     return int(lib().upipe_chunked_workspace_bytes(*sh.args()[:7], n_chunks, 1 if backward else 0))
+
+
+def choose_chunks(sh: Shape, budget_bytes) -> int:
+    """Fewest sequence chunks whose chunked workspaces fit budget_bytes (0 if
+    none); see upipe_choose_chunks."""
+    return int(lib().upipe_choose_chunks(*sh.args()[:7], int(budget_bytes)))
 
 
 def chunked_store_bytes(sh: Shape, n_chunks, backward) -> int:

@@ -1629,6 +1629,16 @@ int upipe_choose_u(int S, int d_model, int H, int G, int d_head, int C, int sche
   return best;
 }
 
+int upipe_choose_chunks(int S, int d_model, int H, int G, int d_head, int U, int C, size_t budget_bytes) {
+  for (int n = 1; n <= S / 128; ++n) {
+    const Shape s{S, d_model, H, G, d_head, U, C, UPIPE_SCHED_INORDER};
+    if (check_chunks(s, n) != UPIPE_OK) continue;
+    const size_t need = std::max(make_chunk_plan(s, n, false).total, make_chunk_plan(s, n, true).total);
+    if (need <= budget_bytes) return n;
+  }
+  return 0;
+}
+
 int upipe_attention_fwd(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf16* V, int n_q, int n_kv, int S,
                         int d_head, const int32_t* kv_of_q, upipe_bf16* O, float* lse, void* stream) {
   const void* ptrs[] = {Q, K, V, O, lse};

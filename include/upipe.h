@@ -182,6 +182,14 @@ size_t upipe_chunked_workspace_bytes(int S, int d_model, int H, int G, int d_hea
                                      int backward);
 size_t upipe_chunked_store_bytes(int S, int d_model, int H, int G, int d_head, int U, int C, int n_chunks,
                                  int backward);
+/*
+ * Chunk-count chooser for the calls below: the smallest n_chunks (the longest
+ * chunks, so the fewest and largest launches) for which both
+ * upipe_chunked_workspace_bytes(..., 0) and (..., 1) are at most
+ * budget_bytes; 0 if no valid count fits.  The store is not counted (it may
+ * live in host memory).  Host only.
+ */
+int upipe_choose_chunks(int S, int d_model, int H, int G, int d_head, int U, int C, size_t budget_bytes);
 int upipe_attn_fwd_chunked(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model,
                            int H, int G, int d_head, int U, int C, int n_chunks, upipe_bf16* Y, upipe_bf16* O_saved,
                            float* lse, void* ws, size_t ws_bytes, void* store, size_t store_bytes, void* stream,

@@ -254,3 +254,22 @@ def test_chunked_sizes_reject_bad_chunk_counts(upipe):
     assert upipe.chunked_workspace_bytes(odd, 8, False) > 0      # 384-token chunks do (128 each)
     gqa = upipe.Shape(1024, 512, 8, 2, 64, 2, 2, upipe.GQA_OUT_OF_ORDER)
     assert upipe.chunked_workspace_bytes(gqa, 2, False) > 0      # the schedule argument is not taken: in order
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b_32k", "llama3_8b_256k_usweep"])
+def test_choose_chunks_is_the_fewest_that_fit(upipe, name):
+    """Against a scan of every chunk count: the chooser returns the smallest
+    valid count whose forward and backward workspaces both fit."""
+    from synthetic import SHAPES
+    s = SHAPES[name]
+    sh = upipe.Shape(s.S, s.d_model, s.H, s.G, s.d_head, s.U, s.C, upipe.IN_ORDER)
+    needs = {}
+    for n in range(1, s.S // 128 + 1):
+        f = upipe.chunked_workspace_bytes(sh, n, False)
+        b = upipe.chunked_workspace_bytes(sh, n, True)
+        if f and b:
+            needs[n] = max(f, b)
+    assert needs
+    for budget in sorted(set(needs.values())) + [min(needs.values()) - 1, 10 ** 15]:
+        want = min((n for n, v in needs.items() if v <= budget), default=0)
+        assert upipe.choose_chunks(sh, budget) == want
