@@ -30,7 +30,7 @@ Sources (page title and section):
 [U3] Same title, arXiv abstract (fugumt.com): chunking at the attention
      head level; up to 87.5% less intermediate memory for 32B models.
 
-Readings where the pages are silent or garbled (each listed in the design doc):
+Readings where the pages are silent or garbled:
   * attention is softmax(Q K^T / sqrt(d_head) + causal mask) V with key j
     visible to query i iff j <= i; no bias, positional rotation or dropout;
   * query head h uses KV head h // (H/G) (contiguous groups);
