@@ -311,13 +311,13 @@ __global__ void __launch_bounds__(512, 1)
         const float* lse = s_lse + st * BQ + half * 64;
         const float* Dv = s_D + st * BQ + half * 64;
         uint32_t pk[32];  // P^T of query columns [64*half, 64*half+64) as bf16 pairs
+        {
+          // this half row of S^T in one load (one wait)
+          uint32_t v[64];
+          tmem_ld64(tmem + lane_off + C::T_S + half * 64, v);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + C::T_S + half * 64 + c * 32, v);
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const int q0 = c * 32 + e;  // within this half
+          for (int q0 = 0; q0 < 64; q0 += 4) {  // within this half
+            const int e = q0;
             const float4 l4 = *reinterpret_cast<const float4*>(lse + q0);
             const uint64_t xa = fma2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, f2(l4.x, l4.y));
             const uint64_t xb = fma2(f2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), sl2x2, f2(l4.z, l4.w));
