@@ -18,6 +18,14 @@
  * The C ranks are virtual: their buffers sit side by side in one GPU's memory
  * and the all-to-all is a device permute with the same index map.
  *
+ * Beyond the plain layer calls (each documented at its declaration): the next
+ * stage's projection overlapped with the current attention
+ * (upipe_fwd_workspace_bytes_prefetch), CUDA-graph replay for short sequences
+ * (upipe_graphs_enable), stage-width and chunk-count choosers for a memory
+ * budget (upipe_choose_u, upipe_choose_chunks), head stages on sequence
+ * chunks with an offload store (upipe_attn_fwd_chunked / _bwd_chunked) and
+ * FP8 scores for chosen stages (upipe_attn_fwd_fp8).
+ *
  * Conventions for every call:
  *   - All tensors are row-major.  bf16 values are passed as upipe_bf16 bit
  *     patterns; fp32 as float.
@@ -27,7 +35,9 @@
  *     log of each causal softmax row's normaliser (scores scaled 1/sqrt(d_head)).
  *   - Pointers named as device pointers must be device memory the caller owns
  *     and 16-byte aligned.  The library never allocates device memory and keeps
- *     no pointer after a call returns.  Work is ordered on `stream` (a
+ *     no pointer after a call returns (except the graphs of
+ *     upipe_graphs_enable, which hold the pointers of the calls they captured
+ *     until graphs are turned off).  Work is ordered on `stream` (a
  *     cudaStream_t; NULL is the legacy default stream); calls return once the
  *     work is enqueued.  Two calls may run concurrently only with distinct
  *     workspaces and outputs.
