@@ -49,3 +49,22 @@ def test_single_process_fallbacks():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.aggregate_tokens_per_s(1, 100, 4, 2000.0) == pytest.approx(200.0)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """The reference arm times the oracle on the host cores and prints one JSON
+    line with the contract's keys (small sample so the test stays fast)."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                        "--steps", "1", "--warmup", "0", "--ref-sample-tokens", "256"],
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
+    assert line["higher_is_better"] is True and line["config"]["workload"] == "tiny"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
