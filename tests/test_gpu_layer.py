@@ -168,6 +168,26 @@ def test_llama_32k_sampled_rows(up):
         assert np.abs(f64_of(lse)[:, rows] - lser).max() < LSE_TOL
 
 
+def test_llama_32k_backward_weight_gradient_identity(up):
+    """Full-size backward (the benchmarked configuration): dW_o is O_saved^T dY
+    by definition, at any size; the library's split-K GEMM over K = S = 32768
+    must match an fp32 product of the same bf16 operands.  dX and dW_qkv must be
+    finite and nonzero."""
+    import torch
+    sh = SHAPES["llama3_8b_32k"]
+    bits = layer_inputs(sh, 0)
+    dev = {k: to_dev(v) for k, v in bits.items()}
+    s = up.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, sh.U, sh.C, 0)
+    Y, O, lse, _ = up.attn_fwd(dev["X"], dev["W_qkv"], dev["W_o"], s)
+    dX, dWq, dWo, _ = up.attn_bwd(dev["X"], dev["W_qkv"], dev["W_o"], O, lse, dev["dY"], s)
+    torch.cuda.synchronize()
+    up.sync_status()
+    ref = O.float().t() @ dev["dY"].float()
+    assert float((dWo - ref).norm() / ref.norm()) < 1e-4
+    for t in (dX.float(), dWq):
+        assert bool(torch.isfinite(t).all()) and float(t.norm()) > 0
+
+
 def _sampled_rows_check(up, name, sched, rows):
     import torch
     sh = SHAPES[name]
