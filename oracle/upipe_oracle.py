@@ -272,6 +272,43 @@ def layer_backward(X, W_qkv, W_o, H, G, d_head, dY):
     return dX, dW_qkv, dW_o
 
 
+def layer_backward_rows(X, W_qkv, W_o, H, G, d_head, dY, rows):
+    """dX at the given rows only (exact).  Row t of dX needs dQ of query t
+    (keys 0..t) and dK, dV of key t, which only the queries i >= t reach, so
+    rows near the end of the sequence are cheap: each query i >= min(rows) is
+    processed once, with its softmax row over keys 0..i."""
+    rows = np.asarray(rows, dtype=np.int64)
+    S = X.shape[0]
+    d = d_head
+    t0 = int(rows.min())
+    Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
+    K = [X @ Wk[g] for g in range(G)]
+    V = [X @ Wv[g] for g in range(G)]
+    dX = np.zeros((len(rows), X.shape[1]))
+    dK = np.zeros((G, len(rows), d))
+    dV = np.zeros((G, len(rows), d))
+    for h in range(H):
+        g = kv_head(h, H, G)
+        Wo_h = W_o[h * d:(h + 1) * d, :]
+        for i in range(t0, S):
+            q = X[i] @ Wq[h]
+            s = K[g][:i + 1] @ q / np.sqrt(d)
+            e = np.exp(s - s.max())
+            p = e / e.sum()
+            o = p @ V[g][:i + 1]
+            do = dY[i] @ Wo_h.T
+            dA = p * (V[g][:i + 1] @ do - do @ o)
+            for r, t in enumerate(rows):
+                if t <= i:  # key t is visible to query i
+                    dK[g, r] += dA[t] * q / np.sqrt(d)
+                    dV[g, r] += p[t] * do
+                if t == i:
+                    dX[r] += (dA @ K[g][:i + 1] / np.sqrt(d)) @ Wq[h].T
+    for g in range(G):
+        dX += dK[g] @ Wk[g].T + dV[g] @ Wv[g].T
+    return dX
+
+
 def layer_forward_rows(X, W_qkv, W_o, H, G, d_head, rows):
     """Y at the given query positions only (exact: each row needs keys 0..row)."""
     rows = np.asarray(rows, dtype=np.int64)

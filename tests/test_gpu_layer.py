@@ -168,11 +168,11 @@ def test_llama_32k_sampled_rows(up):
         assert np.abs(f64_of(lse)[:, rows] - lser).max() < LSE_TOL
 
 
-def test_llama_32k_backward_weight_gradient_identity(up):
+def test_llama_32k_backward_full_size(up):
     """Full-size backward (the benchmarked configuration): dW_o is O_saved^T dY
     by definition, at any size; the library's split-K GEMM over K = S = 32768
-    must match an fp32 product of the same bf16 operands.  dX and dW_qkv must be
-    finite and nonzero."""
+    must match an fp32 product of the same bf16 operands.  dX and dW_qkv are
+    finite and nonzero, and dX on the last rows matches the oracle."""
     import torch
     sh = SHAPES["llama3_8b_32k"]
     bits = layer_inputs(sh, 0)
@@ -186,6 +186,15 @@ def test_llama_32k_backward_weight_gradient_identity(up):
     assert float((dWo - ref).norm() / ref.norm()) < 1e-4
     for t in (dX.float(), dWq):
         assert bool(torch.isfinite(t).all()) and float(t.norm()) > 0
+    # dX on the last rows against the row-wise oracle (exact: the K/V
+    # gradients of those rows come only from the queries after them)
+    rows = np.array([sh.S - 40, sh.S - 2, sh.S - 1])
+    got = f64_of(dX[torch.as_tensor(rows, device="cuda")])
+    del Y, O, lse, dX, dWq, dWo, ref, dev
+    torch.cuda.empty_cache()
+    f = {k: bf16_bits_to_f64(bits[k]) for k in ("X", "W_qkv", "W_o", "dY")}
+    want = orc.layer_backward_rows(f["X"], f["W_qkv"], f["W_o"], sh.H, sh.G, sh.d_head, f["dY"], rows)
+    assert rel(got, want) <= TOL
 
 
 def _sampled_rows_check(up, name, sched, rows):

@@ -229,3 +229,18 @@ def test_attention_rows_match_the_whole_head():
     ro, rl, rdq = orc.attention_rows(q, k, v, do, rows)
     assert np.abs(ro - o[rows]).max() < 1e-13 and np.abs(rl - l[rows]).max() < 1e-13
     assert np.abs(rdq - dq[rows]).max() < 1e-13
+
+
+def test_layer_backward_rows_match_the_whole_layer():
+    """The row-wise dX (used to check full-size backward launches on the last
+    rows) against the whole-layer oracle on every row of a small case."""
+    rng = np.random.default_rng(10)
+    S, dm, H, G, d = 24, 10, 4, 2, 6
+    X = rng.standard_normal((S, dm))
+    W_qkv = rng.standard_normal((dm, (H + 2 * G) * d)) / np.sqrt(dm)
+    W_o = rng.standard_normal((H * d, dm)) / np.sqrt(dm)
+    dY = rng.standard_normal((S, dm))
+    dX, _, _ = orc.layer_backward(X, W_qkv, W_o, H, G, d, dY)
+    for rows in ([S - 1], [S - 1, S - 2, 17], [0, 5, S - 1]):
+        got = orc.layer_backward_rows(X, W_qkv, W_o, H, G, d, dY, rows)
+        assert np.abs(got - dX[rows]).max() < 1e-12
