@@ -273,3 +273,39 @@ def test_choose_chunks_is_the_fewest_that_fit(upipe, name):
     for budget in sorted(set(needs.values())) + [min(needs.values()) - 1, 10 ** 15]:
         want = min((n for n, v in needs.items() if v <= budget), default=0)
         assert upipe.choose_chunks(sh, budget) == want
+
+
+def test_library_accepts_exactly_the_method_shapes_within_its_tiling(upipe):
+    """On random shapes, the library's workspace sizes are nonzero exactly when
+    the oracle's method constraints hold and the kernels' tiling limits are
+    met (S and d_model multiples of 128, d_head 64 or 128, a stage's heads
+    within the slot tables)."""
+    rng = np.random.default_rng(21)
+    seen_ok = seen_bad = 0
+    for _ in range(3000):
+        H = int(rng.choice([4, 6, 8, 12, 16, 32, 64]))
+        G = int(rng.choice([1, 2, 3, 4, 8, 16]))
+        U = int(rng.choice([1, 2, 3, 4, 6, 8, 16, 32]))
+        C = int(rng.choice([1, 2, 3, 4, 8]))
+        S = int(rng.choice([128, 384, 1000, 1024, 1536, 4096]))
+        dm = int(rng.choice([128, 192, 256, 512]))
+        d = int(rng.choice([64, 96, 128]))
+        sched = int(rng.integers(0, 2))
+        try:
+            orc.check_shape(S, dm, H, G, d, U, C, sched)
+            method_ok = True
+        except ValueError:
+            method_ok = False
+        # a stage's exchanged heads (queries plus the K and V heads it moves)
+        # fit the 256-entry slot and 64-column-block tables
+        kv = max(G, C) if sched else min(U, G)
+        cols = U + 2 * max(kv, G if sched else 0)
+        tiling_ok = (S % 128 == 0 and dm % 128 == 0 and d in (64, 128) and 3 * U <= 256 and U + 2 * kv <= 256
+                     and cols * d // 64 <= 256)
+        got = upipe.fwd_workspace_bytes(upipe.Shape(S, dm, H, G, d, U, C, sched)) > 0
+        assert got == (method_ok and tiling_ok), (S, dm, H, G, d, U, C, sched)
+        if got:
+            seen_ok += 1
+        else:
+            seen_bad += 1
+    assert seen_ok > 100 and seen_bad > 100
