@@ -575,12 +575,10 @@ __global__ void __launch_bounds__(256) dq_tiled_to_seq_kernel(const DqTiledDesc 
 template <int D, bool GEN>
 cudaError_t run_bwd(const CUtensorMap* tm, const BwdArgs& args, cudaStream_t st) {
   auto kern = attn_bwd_kernel<D, GEN>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // the kernel needs more than the default 48 KB of dynamic shared memory;
+  // the limit is raised once per device
+  if (const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), BwdCfg<D>::SMEM); e != cudaSuccess)
+    return e;
   kern<<<args.n_kvslots * args.kv_blocks * args.q_split, 512, BwdCfg<D>::SMEM, st>>>(tm[0], tm[1], tm[2], tm[3], tm[4],
                                                                                       args);
   return cudaGetLastError();

@@ -411,12 +411,10 @@ template <int D, bool F8, bool GEN>
 cudaError_t run_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
                     cudaStream_t st) {
   auto kern = attn_fwd_kernel<D, F8, GEN>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D, F8>::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // the kernel needs more than the default 48 KB of dynamic shared memory;
+  // the limit is raised once per device
+  if (const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), FwdCfg<D, F8>::SMEM); e != cudaSuccess)
+    return e;
   kern<<<args.n_qslots * args.q_pairs, 384, FwdCfg<D, F8>::SMEM, st>>>(tq, tk, tv, args);
   return cudaGetLastError();
 }

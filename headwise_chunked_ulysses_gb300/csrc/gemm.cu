@@ -475,12 +475,10 @@ template <bool A_MN, bool B_MN>
 cudaError_t run2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const GemmArgs& args,
                  cudaStream_t st) {
   auto kern = gemm2_kernel<A_MN, B_MN>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // the kernel needs more than the default 48 KB of dynamic shared memory;
+  // the limit is raised once per device
+  if (const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), Cfg2::SMEM); e != cudaSuccess)
+    return e;
   const int tiles = args.m_tiles * args.n_tiles * args.split_k;
   const int pairs = std::min(tiles, num_sms() / 2);
   cudaLaunchConfig_t cfg = {};
@@ -501,12 +499,10 @@ cudaError_t run2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap
 template <int BN, bool A_MN, bool B_MN>
 cudaError_t run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, cudaStream_t st) {
   auto kern = gemm_kernel<BN, A_MN, B_MN>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // the kernel needs more than the default 48 KB of dynamic shared memory;
+  // the limit is raised once per device
+  if (const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), Cfg<BN>::SMEM); e != cudaSuccess)
+    return e;
   const int tiles = args.m_tiles * args.n_tiles * args.split_k;
   const int grid = std::min(tiles, num_sms());
   kern<<<grid, 256, Cfg<BN>::SMEM, st>>>(ta, tb, args);

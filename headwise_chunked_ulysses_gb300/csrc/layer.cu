@@ -31,17 +31,48 @@ namespace upipe {
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
-int g_num_sms = 0;
 __device__ int g_status_word;
-int* g_status_ptr = nullptr;
+
+// Facts the library needs about each device, looked up once per device with
+// that device current: a __device__ variable has one instance per device, so
+// its address (like the SM count and the architecture) is a per-device fact.
+constexpr int kMaxDevices = 64;
+struct DeviceFacts {
+  bool probed = false;
+  bool supported = false;  // compute capability 10.3 (sm_103)
+  int sms = 0;
+  int* status = nullptr;   // this device's instance of g_status_word
+  std::vector<const void*> smem_configured;  // kernels whose shared-memory limit is raised
+};
+std::mutex g_dev_mu;
+DeviceFacts g_dev[kMaxDevices];
+
+// The current device's facts (nullptr if the device cannot be queried).
+// Caller holds g_dev_mu.
+DeviceFacts* facts_locked() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceFacts& f = g_dev[dev];
+  if (!f.probed) {
+    int major = 0, minor = 0, sms = 0;
+    void* p = nullptr;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess)
+      return nullptr;  // not cached: the next call asks again
+    f.supported = (major == 10 && minor == 3);
+    f.sms = sms > 0 ? sms : 1;
+    f.status = static_cast<int*>(p);
+    f.probed = true;
+  }
+  return &f;
+}
 
 int* status_ptr() {
-  if (!g_status_ptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-    g_status_ptr = static_cast<int*>(p);
-  }
-  return g_status_ptr;
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  const DeviceFacts* f = facts_locked();
+  return f ? f->status : nullptr;
 }
 }  // namespace
 
@@ -88,29 +119,29 @@ bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
 int* device_status_word() { return status_ptr(); }
 
 int num_sms() {
-  if (!g_num_sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 1;
-  }
-  return g_num_sms;
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  const DeviceFacts* f = facts_locked();
+  return f ? f->sms : 1;
+}
+
+cudaError_t ensure_dynamic_smem(const void* kernel, int bytes) {
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  DeviceFacts* f = facts_locked();
+  if (!f) return cudaErrorInvalidDevice;
+  for (const void* k : f->smem_configured)
+    if (k == kernel) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) f->smem_configured.push_back(kernel);
+  return e;
+}
+
+bool device_supported() {
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  const DeviceFacts* f = facts_locked();
+  return f && f->supported;
 }
 
 namespace {
-
-bool device_supported() {
-  static int ok = -1;
-  if (ok < 0) {
-    int dev = 0, major = 0, minor = 0;
-    ok = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess)
-      ok = (major == 10 && minor == 3) ? 1 : 0;
-  }
-  return ok == 1;
-}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -543,6 +574,54 @@ int common_checks(const Shape& s, const void* const* ptrs, int n_ptrs, const voi
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// attention backward of one stage's heads: the body shared by the entry point
+// that takes a workspace and the one whose scratch is a fixed array
+// ---------------------------------------------------------------------------
+size_t attention_bwd_scratch_bytes(int n_q, int S) {
+  return 8ull * static_cast<unsigned long long>(n_q) * static_cast<unsigned long long>(S);
+}
+
+int attention_bwd_check(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* lse,
+                        int n_q, int n_kv, int S, int d_head, const int32_t* kv_of_q, const float* dQ,
+                        const float* dK, const float* dV) {
+  const void* ptrs[] = {Q, K, V, O, dO, lse, dQ, dK, dV};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return UPIPE_EINVAL;
+  if (!kv_of_q || n_q <= 0 || n_kv <= 0 || S <= 0 || S % 128) return UPIPE_EINVAL;
+  if (d_head != 64 && d_head != 128) return UPIPE_EUNSUPPORTED;
+  if (n_q > kMaxSlots) return UPIPE_EUNSUPPORTED;
+  for (int k = 0; k < n_q; ++k)
+    if (kv_of_q[k] < 0 || kv_of_q[k] >= n_kv) return UPIPE_EINVAL;
+  return UPIPE_OK;
+}
+
+int attention_bwd_enqueue(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                          const float* lse, int n_q, int n_kv, int S, int d_head, const int32_t* kv_of_q, float* dQ,
+                          float* dK, float* dV, void* scratch, cudaStream_t st) {
+  if (!device_supported()) return UPIPE_EUNSUPPORTED;
+  int* status = status_ptr();
+  if (!status) return UPIPE_ECUDA;
+  float* dsum = static_cast<float*>(scratch);
+  float* lse2 = dsum + static_cast<size_t>(n_q) * S;
+  BwdPrepDesc pr;
+  pr.dO = static_cast<const uint16_t*>(dO); pr.ld_do = d_head; pr.O = static_cast<const uint16_t*>(O);
+  pr.ld_o = d_head; pr.lse = lse;
+  pr.Dsum = dsum; pr.lse2 = lse2; pr.dQacc = dQ; pr.S = S; pr.D = d_head; pr.n_slots = n_q;
+  for (int k = 0; k < n_q; ++k) {
+    pr.do_unit[k] = k * S;
+    pr.o_unit[k] = k * S;
+    pr.lse_row[k] = static_cast<uint16_t>(k);
+  }
+  if (launch_bwd_prep(pr, st) != cudaSuccess) return UPIPE_ECUDA;
+  AttnBwdDesc ab;
+  ab.Q = Q; ab.K = K; ab.V = V; ab.dO = dO; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dQ; ab.dK = dK; ab.dV = dV;
+  ab.accumulate_kv = 0; ab.S = S; ab.D = d_head; ab.n_qslots = n_q; ab.n_kvslots = n_kv;
+  for (int k = 0; k < n_q; ++k) ab.kv_slot[k] = static_cast<uint16_t>(kv_of_q[k]);
+  return launch_attn_bwd(ab, status, st) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
+}
+
 }  // namespace upipe
 
 using namespace upipe;
@@ -980,6 +1059,29 @@ int upipe_layout_head2seq(const upipe_bf16* src, upipe_bf16* dst, int S, int n_h
   return launch_head2seq(h, static_cast<cudaStream_t>(stream)) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
 }
 
+int upipe_layout_head2seq_sum(const float* src, int n_src, const int32_t* head_of_src, upipe_bf16* dst, int S,
+                              int n_heads, int d_head, int dst_row_stride, void* stream) {
+  if (!src || !dst || !head_of_src || !aligned16(src) || !aligned16(dst)) return UPIPE_EINVAL;
+  if (S <= 0 || n_src <= 0 || n_heads <= 0 || d_head <= 0 || d_head % 8 || dst_row_stride % 8 ||
+      dst_row_stride < static_cast<long long>(n_heads) * d_head)
+    return UPIPE_EINVAL;
+  if (n_src > kMaxSlots || n_heads > kMaxSlots) return UPIPE_EUNSUPPORTED;
+  Head2SeqDesc h;
+  h.src = src; h.src_f32 = true; h.dst = dst; h.ld_dst = dst_row_stride; h.S = S; h.D = d_head; h.n_heads = n_heads;
+  // CSR of the source slots of each output head, ascending slot order
+  int n = 0;
+  for (int k = 0; k < n_heads; ++k) {
+    h.dst_head[k] = static_cast<uint16_t>(k);
+    h.first[k] = static_cast<uint16_t>(n);
+    for (int j = 0; j < n_src; ++j)
+      if (head_of_src[j] == k) h.src_slot[n++] = static_cast<uint16_t>(j);
+    if (n == h.first[k]) return UPIPE_EINVAL;  // an output head without a source
+  }
+  if (n != n_src) return UPIPE_EINVAL;  // a source slot naming no output head
+  h.first[n_heads] = static_cast<uint16_t>(n);
+  return launch_head2seq(h, static_cast<cudaStream_t>(stream)) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
+}
+
 int upipe_schedule_table(int H, int G, int U, int C, int sched, int32_t* host_out) {
   const Shape s{128 * (C > 0 ? C : 1), 128, H, G, 64, U, C, sched};  // only H, G, U, C matter here
   if (!host_out) return UPIPE_EINVAL;
@@ -1106,35 +1208,12 @@ int upipe_attention_bwd(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf
                         const upipe_bf16* dO, const float* lse, int n_q, int n_kv, int S, int d_head,
                         const int32_t* kv_of_q, float* dQ, float* dK, float* dV, void* ws, size_t ws_bytes,
                         void* stream) {
-  const void* ptrs[] = {Q, K, V, O, dO, lse, dQ, dK, dV, ws};
-  for (const void* q : ptrs)
-    if (!q || !aligned16(q)) return UPIPE_EINVAL;
-  if (!kv_of_q || n_q <= 0 || n_kv <= 0 || S <= 0 || S % 128) return UPIPE_EINVAL;
-  if (d_head != 64 && d_head != 128) return UPIPE_EUNSUPPORTED;
-  if (n_q > kMaxSlots) return UPIPE_EUNSUPPORTED;
-  for (int k = 0; k < n_q; ++k)
-    if (kv_of_q[k] < 0 || kv_of_q[k] >= n_kv) return UPIPE_EINVAL;
-  if (ws_bytes < 8ull * n_q * S) return UPIPE_ENOSPC;
-  if (!device_supported()) return UPIPE_EUNSUPPORTED;
-  int* status = status_ptr();
-  if (!status) return UPIPE_ECUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float* dsum = static_cast<float*>(ws);
-  float* lse2 = dsum + static_cast<size_t>(n_q) * S;
-  BwdPrepDesc pr;
-  pr.dO = dO; pr.ld_do = d_head; pr.O = O; pr.ld_o = d_head; pr.lse = lse;
-  pr.Dsum = dsum; pr.lse2 = lse2; pr.dQacc = dQ; pr.S = S; pr.D = d_head; pr.n_slots = n_q;
-  for (int k = 0; k < n_q; ++k) {
-    pr.do_unit[k] = k * S;
-    pr.o_unit[k] = k * S;
-    pr.lse_row[k] = static_cast<uint16_t>(k);
-  }
-  if (launch_bwd_prep(pr, st) != cudaSuccess) return UPIPE_ECUDA;
-  AttnBwdDesc ab;
-  ab.Q = Q; ab.K = K; ab.V = V; ab.dO = dO; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dQ; ab.dK = dK; ab.dV = dV;
-  ab.accumulate_kv = 0; ab.S = S; ab.D = d_head; ab.n_qslots = n_q; ab.n_kvslots = n_kv;
-  for (int k = 0; k < n_q; ++k) ab.kv_slot[k] = static_cast<uint16_t>(kv_of_q[k]);
-  return launch_attn_bwd(ab, status, st) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
+  const int rc = attention_bwd_check(Q, K, V, O, dO, lse, n_q, n_kv, S, d_head, kv_of_q, dQ, dK, dV);
+  if (rc != UPIPE_OK) return rc;
+  if (!ws || !aligned16(ws)) return UPIPE_EINVAL;
+  if (ws_bytes < attention_bwd_scratch_bytes(n_q, S)) return UPIPE_ENOSPC;
+  return attention_bwd_enqueue(Q, K, V, O, dO, lse, n_q, n_kv, S, d_head, kv_of_q, dQ, dK, dV, ws,
+                               static_cast<cudaStream_t>(stream));
 }
 
 int upipe_gemm_bf16(const upipe_bf16* A, const upipe_bf16* B, void* D, int M, int N, int K, int a_trans, int b_trans,

@@ -56,8 +56,6 @@ cudaError_t scratch_for_current_device(void** scratch) {
   return cudaSuccess;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 }  // namespace upipe
 
@@ -67,42 +65,13 @@ extern "C" int upipe_attention_bwd_noalloc(const upipe_bf16* Q, const upipe_bf16
                                            const upipe_bf16* O, const upipe_bf16* dO, const float* lse, int n_q,
                                            int n_kv, int S, int d_head, const int32_t* kv_of_q, float* dQ,
                                            float* dK, float* dV, void* stream) {
-  const void* ptrs[] = {Q, K, V, O, dO, lse, dQ, dK, dV};
-  for (const void* q : ptrs)
-    if (!q || !aligned16(q)) return UPIPE_EINVAL;
-  if (!kv_of_q || n_q <= 0 || n_kv <= 0 || S <= 0 || S % 128) return UPIPE_EINVAL;
-  if (d_head != 64 && d_head != 128) return UPIPE_EUNSUPPORTED;
-  if (n_q > kMaxSlots) return UPIPE_EUNSUPPORTED;
-  for (int k = 0; k < n_q; ++k)
-    if (kv_of_q[k] < 0 || kv_of_q[k] >= n_kv) return UPIPE_EINVAL;
+  const int rc = attention_bwd_check(Q, K, V, O, dO, lse, n_q, n_kv, S, d_head, kv_of_q, dQ, dK, dV);
+  if (rc != UPIPE_OK) return rc;
   // the fixed scratch holds D and lse*log2(e) for every (query slot, token)
-  if (8ull * static_cast<unsigned long long>(n_q) * static_cast<unsigned long long>(S) > kNoAllocScratchBytes)
-    return UPIPE_ENOSPC;
-  int dev = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return UPIPE_ECUDA;
-  if (major != 10 || minor != 3) return UPIPE_EUNSUPPORTED;
+  if (attention_bwd_scratch_bytes(n_q, S) > kNoAllocScratchBytes) return UPIPE_ENOSPC;
+  if (!device_supported()) return UPIPE_EUNSUPPORTED;
   void* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return UPIPE_ECUDA;
-  int* status = device_status_word();  // the word upipe_sync_status() reads
-  if (!status) return UPIPE_ECUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float* dsum = static_cast<float*>(scratch);
-  float* lse2 = dsum + static_cast<size_t>(n_q) * S;
-  BwdPrepDesc pr;
-  pr.dO = dO; pr.ld_do = d_head; pr.O = O; pr.ld_o = d_head; pr.lse = lse;
-  pr.Dsum = dsum; pr.lse2 = lse2; pr.dQacc = dQ; pr.S = S; pr.D = d_head; pr.n_slots = n_q;
-  for (int k = 0; k < n_q; ++k) {
-    pr.do_unit[k] = k * S;
-    pr.o_unit[k] = k * S;
-    pr.lse_row[k] = static_cast<uint16_t>(k);
-  }
-  if (launch_bwd_prep(pr, st) != cudaSuccess) return UPIPE_ECUDA;
-  AttnBwdDesc ab;
-  ab.Q = Q; ab.K = K; ab.V = V; ab.dO = dO; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dQ; ab.dK = dK; ab.dV = dV;
-  ab.accumulate_kv = 0; ab.S = S; ab.D = d_head; ab.n_qslots = n_q; ab.n_kvslots = n_kv;
-  for (int k = 0; k < n_q; ++k) ab.kv_slot[k] = static_cast<uint16_t>(kv_of_q[k]);
-  return launch_attn_bwd(ab, status, st) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
+  return attention_bwd_enqueue(Q, K, V, O, dO, lse, n_q, n_kv, S, d_head, kv_of_q, dQ, dK, dV, scratch,
+                               static_cast<cudaStream_t>(stream));
 }

@@ -166,8 +166,29 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
                   uint32_t box_inner, uint32_t box_outer);
 bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_elems,
                    uint32_t box_inner, uint32_t box_outer);
+// Facts of the current device, looked up once per device with it current.
 int num_sms();
-// Device address of the status word bounded waits write (read by upipe_sync_status).
+bool device_supported();  // compute capability 10.3
+// Device address of the current device's status word that bounded waits
+// write (read and cleared by upipe_sync_status).
 int* device_status_word();
+// Raises a kernel's dynamic shared-memory limit on the current device (once
+// per device and kernel).
+cudaError_t ensure_dynamic_smem(const void* kernel, int bytes);
+
+// The attention backward of one stage's heads in head layout, shared by
+// upipe_attention_bwd (scratch in the caller's workspace) and
+// upipe_attention_bwd_noalloc (scratch in a fixed array of the library).
+// Scratch: D = rowsum(dO * O) and -lse * log2(e), n_q * S floats each.
+size_t attention_bwd_scratch_bytes(int n_q, int S);
+// Argument checks of the public call (pointers, shape, KV slot map); UPIPE_* code.
+int attention_bwd_check(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* lse,
+                        int n_q, int n_kv, int S, int d_head, const int32_t* kv_of_q, const float* dQ,
+                        const float* dK, const float* dV);
+// Enqueues the preprocessing and the backward kernel on st; arguments already
+// checked; scratch holds attention_bwd_scratch_bytes() bytes of device memory.
+int attention_bwd_enqueue(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                          const float* lse, int n_q, int n_kv, int S, int d_head, const int32_t* kv_of_q, float* dQ,
+                          float* dK, float* dV, void* scratch, cudaStream_t st);
 
 }  // namespace upipe
