@@ -309,6 +309,54 @@ def layer_backward_rows(X, W_qkv, W_o, H, G, d_head, dY, rows):
     return dX
 
 
+def layer_backward_sparse_dy(X, W_qkv, W_o, H, G, d_head, dY_rows, rows):
+    """Every gradient (dX, dW_qkv, dW_o) of L = <Y, dY> for an upstream
+    gradient dY that is zero outside the given query rows, dY[rows] = dY_rows.
+
+    This is ``layer_backward`` with the zero rows left out, not an
+    approximation: a row i with dY[i] = 0 has dO_h[i] = 0 for every head, so
+    its dP row and its D are zero, its dA row is zero, and it adds nothing to
+    dV = P^T dO, dK = dA^T q, dQ or dW_o = O^T dY.  Only the softmax rows of
+    the listed queries are formed (each over keys 0..i), so the cost is
+    |rows| x S per head instead of S x S, and the full-length K/V gradients,
+    dW_qkv and every row of dX still come out exact."""
+    rows = np.asarray(rows, dtype=np.int64)
+    S = X.shape[0]
+    d = d_head
+    Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
+    Xr = X[rows]
+    visible = np.arange(S)[None, :] <= rows[:, None]  # key j visible to query rows[r]
+    dX = np.zeros_like(X)
+    dW_qkv = np.zeros_like(W_qkv)
+    O_rows = np.zeros((len(rows), H * d))
+    for g in range(G):
+        K = X @ Wk[g]
+        V = X @ Wv[g]
+        dK = np.zeros((S, d))
+        dV = np.zeros((S, d))
+        for h in range(H):
+            if kv_head(h, H, G) != g:
+                continue
+            q = Xr @ Wq[h]
+            A = np.where(visible, (q @ K.T) / np.sqrt(d), -np.inf)
+            m = A.max(axis=1, keepdims=True)
+            E = np.exp(A - m)
+            P = E / E.sum(axis=1, keepdims=True)
+            o = P @ V
+            O_rows[:, h * d:(h + 1) * d] = o
+            do = dY_rows @ W_o[h * d:(h + 1) * d, :].T
+            dA = P * (do @ V.T - (do * o).sum(axis=1, keepdims=True))
+            dq = dA @ K / np.sqrt(d)
+            dK += dA.T @ q / np.sqrt(d)
+            dV += P.T @ do
+            dW_qkv[:, h * d:(h + 1) * d] = Xr.T @ dq
+            dX[rows] += dq @ Wq[h].T
+        dW_qkv[:, (H + g) * d:(H + g + 1) * d] = X.T @ dK
+        dW_qkv[:, (H + G + g) * d:(H + G + g + 1) * d] = X.T @ dV
+        dX += dK @ Wk[g].T + dV @ Wv[g].T
+    return dX, dW_qkv, O_rows.T @ dY_rows
+
+
 def layer_forward_rows(X, W_qkv, W_o, H, G, d_head, rows):
     """Y at the given query positions only (exact: each row needs keys 0..row)."""
     rows = np.asarray(rows, dtype=np.int64)
@@ -370,6 +418,23 @@ def head_to_seq(held, heads_of, S):
              for c in range(C)] for r in range(C)]
     recv = all_to_all(send)
     return [[pair for blocks in recv[c] for pair in blocks] for c in range(C)]
+
+
+def replica_gradient_sum(copies):
+    """Gradient of a head whose copies several ranks held, in the in-order
+    exchange's backward (reading: every query slot receives its own copy of
+    its KV head, [U1] Method steps (2); the copies' gradients are added in
+    ascending rank order, in fp32).
+
+    copies: [n, S, d] fp32 values, in ascending rank order.  Returns
+    (sum32, rounded): the fp32 running sum copy_0 + copy_1 + ... evaluated
+    left to right with float32 rounding after every addition, and that sum
+    rounded once to bfloat16 (as float64 values)."""
+    c = np.asarray(copies, dtype=np.float32)
+    acc = c[0].copy()
+    for x in c[1:]:
+        acc = (acc + x).astype(np.float32)
+    return acc, bf16_round(acc)
 
 
 # ---------------------------------------------------------------------------

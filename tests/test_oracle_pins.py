@@ -244,3 +244,51 @@ def test_layer_backward_rows_match_the_whole_layer():
     for rows in ([S - 1], [S - 1, S - 2, 17], [0, 5, S - 1]):
         got = orc.layer_backward_rows(X, W_qkv, W_o, H, G, d, dY, rows)
         assert np.abs(got - dX[rows]).max() < 1e-12
+
+
+# --------------------------------------------------------------------------
+# the backward for an upstream gradient that is zero outside a few rows
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H,G,rows", [(4, 2, [0, 7, 8, 25, 39]), (4, 4, [39]), (4, 1, [0]),
+                                      (6, 3, [3, 4, 5, 17, 30, 31])])
+def test_sparse_dy_backward_is_the_whole_layer_backward(H, G, rows):
+    """layer_backward_sparse_dy leaves out only the rows where dY is zero:
+    it must equal the whole-layer backward (pinned by finite differences
+    above) run on dY zeroed outside those rows, for every output."""
+    S, d_model, d = 40, 16, 4
+    X, W_qkv, W_o, dY = _rand_layer(S, d_model, H, G, d, seed=len(rows) + H)
+    rows = np.array(rows)
+    dY_sparse = np.zeros_like(dY)
+    dY_sparse[rows] = dY[rows]
+    want = orc.layer_backward(X, W_qkv, W_o, H, G, d, dY_sparse)
+    got = orc.layer_backward_sparse_dy(X, W_qkv, W_o, H, G, d, dY[rows], rows)
+    for name, a, b in zip(("dX", "dW_qkv", "dW_o"), got, want):
+        assert np.abs(a - b).max() <= 1e-12 * max(1.0, np.abs(b).max()), name
+    # the K/V gradients reach every key row up to the last listed query, and
+    # rows of dX below it are nonzero although dY is zero there
+    assert rows.max() == 0 or np.abs(got[0][: rows.max()]).max() > 0
+
+
+# --------------------------------------------------------------------------
+# fp32 sum of a KV head's gradient copies, in rank order
+# --------------------------------------------------------------------------
+
+def test_replica_gradient_sum_order_and_rounding():
+    e = 2.0 ** -24  # half an fp32 unit at 1.0
+    # left to right: 1 + e rounds back to 1 (tie, even), twice
+    s32, r = orc.replica_gradient_sum([[1.0], [e], [e]])
+    assert s32[0] == np.float32(1.0)
+    # the small copies first: e + e = 2e, then 1 + 2e is exact in fp32
+    s32, r = orc.replica_gradient_sum([[e], [e], [1.0]])
+    assert s32[0] == np.float32(1.0 + 2 * e)
+    # one copy: just its bf16 rounding; ties go to the even mantissa
+    for x, want in ((1.0 + 2.0 ** -8, 1.0), (1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -6), (-(1.0 + 2.0 ** -8), -1.0),
+                    (1.0 + 2.0 ** -8 + 2.0 ** -20, 1.0 + 2.0 ** -7)):
+        s32, r = orc.replica_gradient_sum([[x]])
+        assert r[0] == want, (x, r[0], want)
+    # small integers add exactly in any order
+    rng = np.random.default_rng(5)
+    c = rng.integers(-50, 50, size=(8, 3, 4)).astype(np.float32)
+    s32, r = orc.replica_gradient_sum(c)
+    assert np.array_equal(s32, c.sum(axis=0)) and np.array_equal(r, c.sum(axis=0).astype(np.float64))
