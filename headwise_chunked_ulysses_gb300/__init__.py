@@ -30,6 +30,7 @@ EXPORTS = (
     "upipe_graphs_enable", "upipe_chunked_workspace_bytes", "upipe_chunked_store_bytes",
     "upipe_attn_fwd_chunked", "upipe_attn_bwd_chunked",
     "upipe_quantize_e4m3", "upipe_attention_fwd_fp8", "upipe_attn_fwd_fp8", "upipe_choose_chunks",
+    "upipe_layout_head2seq_sum", "upipe_watchdog_selftest",
 )
 
 
@@ -73,6 +74,8 @@ def _sig(lib):
         "upipe_attn_bwd": (I, [P, P, P] + [I] * 8 + [P, P, P, P, P, P, P, Z, P, ctypes.POINTER(Stats)]),
         "upipe_layout_seq2head": (I, [P, P, I, I, I, I, I, P]),
         "upipe_layout_head2seq": (I, [P, P, I, I, I, I, I, P]),
+        "upipe_layout_head2seq_sum": (I, [P, I, i32p, P, I, I, I, I, P]),
+        "upipe_watchdog_selftest": (I, [LL, I, P]),
         "upipe_schedule_table": (I, [I, I, I, I, I, i32p]),
         "upipe_choose_u": (I, [I, I, I, I, I, I, I, Z]),
         "upipe_attention_fwd": (I, [P, P, P, I, I, I, I, i32p, P, P, P]),
@@ -376,6 +379,25 @@ def layout_head2seq(src, dst, S, n_heads, d_head, C, dst_row_stride, stream=None
     _check("upipe_layout_head2seq", lib().upipe_layout_head2seq(
         _ptr(src, bf, "src"), _ptr(dst, bf, "dst"), S, n_heads, d_head, C, dst_row_stride, _stream(stream)))
     return dst
+
+
+def layout_head2seq_sum(src, head_of_src, dst, n_heads, dst_row_stride, stream=None):
+    """Gradients in head layout (fp32 [n_src, S, d]) back to bf16 sequence
+    rows, the copies of each head summed in ascending slot order
+    (see upipe_layout_head2seq_sum)."""
+    torch = _torch()
+    n_src, S, d = src.shape
+    _check("upipe_layout_head2seq_sum", lib().upipe_layout_head2seq_sum(
+        _ptr(src, torch.float32, "src"), n_src, _i32(head_of_src), _ptr(dst, torch.bfloat16, "dst"), S, n_heads, d,
+        dst_row_stride, _stream(stream)))
+    return dst
+
+
+def watchdog_selftest(limit_cycles, warp_form=0, stream=None):
+    """Launch the bounded-wait self-test (see upipe_watchdog_selftest); the
+    next sync_status() raises with UPIPE_ETIMEOUT."""
+    _check("upipe_watchdog_selftest", lib().upipe_watchdog_selftest(int(limit_cycles), int(warp_form),
+                                                                    _stream(stream)))
 
 
 def _i32(seq):

@@ -64,14 +64,16 @@ struct Watch {
 };
 
 // Wait until the phase with the given parity has completed.  Returns false
-// (after flagging) if the wait gave up or another thread of the CTA aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Watch& w, int site) {
+// (after flagging) if the wait gave up after `limit` SM clocks or another
+// thread of the CTA aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Watch& w, int site,
+                                          long long limit = UPIPE_WAIT_CYCLES) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(a, parity)) {
     if (*w.abort_flag) return false;
-    if (clock64() - t0 > UPIPE_WAIT_CYCLES) {
+    if (clock64() - t0 > limit) {
       *w.abort_flag = 1;
       if (w.status) atomicCAS(w.status, 0, kDevTimeout | site);
       __threadfence();
@@ -83,7 +85,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 
 // Warp-collective variant: every lane polls, the decision to give up is lane
 // 0's, so the whole warp leaves together (needed before .sync.aligned ops).
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const Watch& w, int site) {
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const Watch& w, int site,
+                                               long long limit = UPIPE_WAIT_CYCLES) {
   const uint32_t a = smem_u32(bar);
   if (__all_sync(0xffffffffu, mbar_try_wait(a, parity))) return true;
   const long long t0 = clock64();
@@ -91,7 +94,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, c
     const bool ok = mbar_try_wait(a, parity);
     if (__all_sync(0xffffffffu, ok)) return true;
     int give_up = 0;
-    if ((threadIdx.x & 31) == 0) give_up = (*w.abort_flag != 0) || (clock64() - t0 > UPIPE_WAIT_CYCLES);
+    if ((threadIdx.x & 31) == 0) give_up = (*w.abort_flag != 0) || (clock64() - t0 > limit);
     give_up = __shfl_sync(0xffffffffu, give_up, 0);
     if (give_up) {
       if ((threadIdx.x & 31) == 0 && !*w.abort_flag) {

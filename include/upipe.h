@@ -228,6 +228,26 @@ int upipe_layout_head2seq(const upipe_bf16* src, upipe_bf16* dst, int S, int n_h
                           int dst_row_stride, void* stream);
 
 /*
+ * The reverse exchange of the backward pass (Method steps (2) and (4) run
+ * backwards): gradients held in head layout return to sequence layout, and
+ * the copies of one head that several ranks hold are summed.  In the in-order
+ * exchange every query slot receives its own copy of its KV head, so the
+ * gradient of that KV head is the sum of the copies' gradients.
+ *   src : device fp32 [n_src][S][d_head], one gradient per source slot.
+ *   head_of_src : HOST int32 [n_src], the output head each source slot
+ *         belongs to; every output head 0..n_heads-1 needs at least one.
+ *   dst : device bf16 rows of dst_row_stride elements; head h of token t at
+ *         dst[t * dst_row_stride + h * d_head ..].
+ * Each output value is the fp32 sum of its sources taken in ascending source
+ * slot order (the first source, plus the second, ...; ascending slot order is
+ * ascending rank order), rounded once to bf16 (nearest, ties to even).  The
+ * result is therefore bit-for-bit reproducible.  d_head % 8 == 0,
+ * dst_row_stride % 8 == 0, n_src and n_heads <= 256.
+ */
+int upipe_layout_head2seq_sum(const float* src, int n_src, const int32_t* head_of_src, upipe_bf16* dst, int S,
+                              int n_heads, int d_head, int dst_row_stride, void* stream);
+
+/*
  * Head schedule (Method steps (1)-(2), Novelty): host_out[(i*C + r)*(U/C) + j]
  * receives the query head that stage i places in slot j of rank r.
  * host_out is HOST memory of H int32 entries.
@@ -349,6 +369,21 @@ int upipe_attention_bwd_noalloc(const upipe_bf16* Q, const upipe_bf16* K, const 
  */
 int upipe_gemm_bf16(const upipe_bf16* A, const upipe_bf16* B, void* D, int M, int N, int K, int a_trans, int b_trans,
                     long long lda, long long ldb, long long ldd, int out_mode, void* stream);
+
+/*
+ * Self-test of the failure detection (no counterpart on the pages): every
+ * wait of the library's kernels on an mbarrier is bounded; when one runs out
+ * the kernel records a timeout in the device status word and exits, and
+ * upipe_sync_status() returns UPIPE_ETIMEOUT.  This call launches one CTA
+ * that waits, with a limit of limit_cycles SM clocks (1000 .. 1e9), on an
+ * mbarrier nothing arrives at -- with the per-thread form of the wait
+ * (warp_form == 0) or the warp-collective form (1) -- so that path runs for
+ * real: nothing else is in flight in that CTA, and it returns within the
+ * limit.  The next upipe_sync_status() reports UPIPE_ETIMEOUT and clears the
+ * word.  UPIPE_EUNSUPPORTED when the library was built without it
+ * (UPIPE_SELFTEST=0).
+ */
+int upipe_watchdog_selftest(long long limit_cycles, int warp_form, void* stream);
 
 /* Reads (and clears) the device status word that bounded waits write; the
  * call synchronises `stream`.  UPIPE_OK or UPIPE_ETIMEOUT. */

@@ -156,6 +156,16 @@ def test_arguments_checked_before_any_launch(upipe):
     rc = lib.upipe_layout_seq2head(fake, fake, 1024, 6, 64, 4, 384, None)
     assert rc == upipe.EINVAL
     assert lib.upipe_status_str(upipe.ETIMEOUT) == b"a kernel wait timed out"
+    # the reverse exchange with replica sums: every output head needs a source
+    # slot and every source slot an output head
+    i32 = lambda xs: (ctypes.c_int32 * len(xs))(*xs)
+    assert lib.upipe_layout_head2seq_sum(fake, 2, i32([0, 2]), fake, 128, 3, 64, 192, None) == upipe.EINVAL
+    assert lib.upipe_layout_head2seq_sum(fake, 2, i32([0, 5]), fake, 128, 1, 64, 64, None) == upipe.EINVAL
+    assert lib.upipe_layout_head2seq_sum(fake, 2, i32([0, 0]), fake, 128, 1, 60, 64, None) == upipe.EINVAL
+    assert lib.upipe_layout_head2seq_sum(fake, 2, i32([0, 0]), fake, 128, 1, 64, 32, None) == upipe.EINVAL
+    # the bounded-wait self-test: limits outside 1000 .. 1e9 cycles, unknown form
+    for limit, form in ((10, 0), (2_000_000_000, 0), (100_000, 2)):
+        assert lib.upipe_watchdog_selftest(limit, form, None) == upipe.EINVAL
 
 
 def _valid_us(upipe, S, dm, H, G, d, C, sched):
@@ -279,13 +289,19 @@ def test_library_accepts_exactly_the_method_shapes_within_its_tiling(upipe):
     """On random shapes, the library's workspace sizes are nonzero exactly when
     the oracle's method constraints hold and the kernels' tiling limits are
     met (S and d_model multiples of 128, d_head 64 or 128, a stage's heads
-    within the slot tables)."""
+    within the 256-entry slot tables and the 256 64-column blocks a gather
+    map names).  Head counts reach 256 so that the limits on 3U slots and on
+    the gather map's blocks are each, on some method-valid draw, the only one
+    broken; U + 2 kv <= 256 slots never breaks alone, since the stage buffer's
+    cols * d / 64 blocks are at least U + 2 kv, but it is seen broken."""
     rng = np.random.default_rng(21)
     seen_ok = seen_bad = 0
-    for _ in range(3000):
-        H = int(rng.choice([4, 6, 8, 12, 16, 32, 64]))
-        G = int(rng.choice([1, 2, 3, 4, 8, 16]))
-        U = int(rng.choice([1, 2, 3, 4, 6, 8, 16, 32]))
+    alone = {"3U": 0, "U+2kv": 0, "cols": 0}
+    broken_kv = 0
+    for _ in range(6000):
+        H = int(rng.choice([4, 6, 8, 12, 16, 32, 64, 96, 128, 192, 256]))
+        G = int(rng.choice([1, 2, 3, 4, 8, 16, 32, 64, 128]))
+        U = int(rng.choice([1, 2, 3, 4, 6, 8, 16, 32, 64, 96, 128, 256]))
         C = int(rng.choice([1, 2, 3, 4, 8]))
         S = int(rng.choice([128, 384, 1000, 1024, 1536, 4096]))
         dm = int(rng.choice([128, 192, 256, 512]))
@@ -300,12 +316,19 @@ def test_library_accepts_exactly_the_method_shapes_within_its_tiling(upipe):
         # fit the 256-entry slot and 64-column-block tables
         kv = max(G, C) if sched else min(U, G)
         cols = U + 2 * max(kv, G if sched else 0)
-        tiling_ok = (S % 128 == 0 and dm % 128 == 0 and d in (64, 128) and 3 * U <= 256 and U + 2 * kv <= 256
-                     and cols * d // 64 <= 256)
+        basic = S % 128 == 0 and dm % 128 == 0 and d in (64, 128)
+        terms = {"3U": 3 * U <= 256, "U+2kv": U + 2 * kv <= 256, "cols": cols * d // 64 <= 256}
+        tiling_ok = basic and all(terms.values())
         got = upipe.fwd_workspace_bytes(upipe.Shape(S, dm, H, G, d, U, C, sched)) > 0
         assert got == (method_ok and tiling_ok), (S, dm, H, G, d, U, C, sched)
+        if method_ok and basic:
+            broken = [k for k, v in terms.items() if not v]
+            if len(broken) == 1:
+                alone[broken[0]] += 1
+            broken_kv += not terms["U+2kv"]
         if got:
             seen_ok += 1
         else:
             seen_bad += 1
     assert seen_ok > 100 and seen_bad > 100
+    assert alone["3U"] > 0 and alone["cols"] > 0 and alone["U+2kv"] == 0 and broken_kv > 0, (alone, broken_kv)
