@@ -112,22 +112,18 @@ def source_sha(kernel):
 
 
 def measured_traffic(kernel, workload):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary
-    profiles/traffic_<kernel>_<workload>.md, if that capture was taken from
+    """DRAM bytes per launch of `kernel` from the committed ncu figure
+    profiles/traffic_<kernel>_<workload>.json, if that capture was taken from
     the current source of the kernel (else None)."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.json")
     if not os.path.exists(path):
         return None
-    fields = {}
-    for line in open(path):
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    if fields.get("source_sha256_16") != source_sha(kernel):
-        return None
     try:
-        return float(fields["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+        rec = json.load(open(path))
+        if rec.get("source_sha256_16") != source_sha(kernel):
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except (ValueError, KeyError, TypeError):
         return None
 
 
@@ -252,29 +248,44 @@ def run_kernel_profile(args, sh):
     return 0
 
 
-def run_sweep(args):
-    """The other workloads: one JSON line each (tokens/s, TFLOP/s, stage-arena
-    bytes against the 12*S*U*d_head form, exchanged bytes).  Not the headline."""
-    import numpy as np
-    import torch
-    import headwise_chunked_ulysses_gb300 as upipe
+DEFAULT_SWEEP = ("llama3_8b_256k_usweep", "qwen3_32b_128k", "llama3_8b_512k_gqa")
+
+
+def sweep_cases(names=None, extra=False):
+    """(workload, shape, schedule, sequence chunks (0: none; -1: FP8 heads),
+    offload store) of the other workloads: the U sweep at 256K, the Qwen3-32B
+    layer at 128K, the 512K layer under both schedules (the GQA schedule's
+    exchange bytes against the in-order ones); with extra, also the sequence-
+    chunked and FP8 rows."""
     from synthetic import SHAPES
-    dev = torch.device("cuda", 0)
-    pk = peaks()
-    cases = []  # (name, shape, schedule, sequence chunks (0: none; -1: FP8 heads), offload store)
+    cases = []
     us = SHAPES["llama3_8b_256k_usweep"]
     for U in (8, 16, 32):
         cases.append(("llama3_8b_256k_usweep", us.replace(U=U), 0, 0, None))
-    gq = SHAPES["llama3_8b_512k_gqa"]
-    cases += [("llama3_8b_512k_gqa", gq, 0, 0, None), ("llama3_8b_512k_gqa", gq, 1, 0, None)]
     cases.append(("qwen3_32b_128k", SHAPES["qwen3_32b_128k"], 0, 0, None))
-    # head stages on sequence chunks, K/V offloaded to page-locked host memory
-    cases += [("llama3_8b_256k_chunked", us, 0, 8, "host"), ("llama3_8b_256k_chunked", us, 0, 16, "host"),
-              ("llama3_8b_512k_chunked", gq, 0, 16, "host")]
-    # every head's scores in FP8 (forward), bf16 backward
-    cases += [("llama3_8b_32k_fp8", SHAPES["llama3_8b_32k"], 0, -1, None), ("llama3_8b_256k_fp8", us, 0, -1, None)]
-    if args.sweep_only:
-        cases = [c for c in cases if c[0] in args.sweep_only.split(",")]
+    gq = SHAPES["llama3_8b_512k_gqa"]
+    cases += [("llama3_8b_512k_gqa", gq, 1, 0, None), ("llama3_8b_512k_gqa", gq, 0, 0, None)]
+    if extra:
+        # head stages on sequence chunks, K/V offloaded to page-locked host memory
+        cases += [("llama3_8b_256k_chunked", us, 0, 8, "host"), ("llama3_8b_256k_chunked", us, 0, 16, "host"),
+                  ("llama3_8b_512k_chunked", gq, 0, 16, "host")]
+        # every head's scores in FP8 (forward), bf16 backward
+        cases += [("llama3_8b_32k_fp8", SHAPES["llama3_8b_32k"], 0, -1, None), ("llama3_8b_256k_fp8", us, 0, -1, None)]
+    if names:
+        cases = [c for c in cases if c[0] in names]
+    return cases
+
+
+def sweep_entries(cases, steps, warmup):
+    """Time each case (warmup untimed steps, then `steps` fwd+bwd steps on the
+    device) and yield one dict per case: tokens/s, TFLOP/s and their fractions
+    of the burst and sustained bf16 peaks, the attention backward kernel's own
+    rate, the stage arenas against the pages' forms, and the exchange bytes."""
+    import numpy as np
+    import torch
+    import headwise_chunked_ulysses_gb300 as upipe
+    dev = torch.device("cuda", 0)
+    pk = peaks()
     for name, sh, sched, n_chunks, where in cases:
         s = upipe.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, sh.U, sh.C, sched)
         g = torch.Generator(device=dev).manual_seed(0)
@@ -317,14 +328,18 @@ def run_sweep(args):
                 return upipe.attn_bwd(X, Wqkv, Wo, O, lse, dY, s, ws=wsb, **kw)
         Y, O, lse, _ = fwd()
         dX, dWqkv, dWo, _ = bwd(O, lse)
+        for _ in range(max(0, warmup - 1)):
+            fwd(Y=Y, O_saved=O, lse=lse)
+            bwd(O, lse, dX=dX, dW_qkv=dWqkv, dW_o=dWo)
         torch.cuda.synchronize()
+        upipe.sync_status()
         clocks = ClockSampler(0)
         clocks.start()
         upipe.profile_enable(True)
         upipe.profile_read()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(args.sweep_steps):
+        for _ in range(steps):
             _, _, _, stf = fwd(Y=Y, O_saved=O, lse=lse)
             _, _, _, stb = bwd(O, lse, dX=dX, dW_qkv=dWqkv, dW_o=dWo)
         e1.record()
@@ -333,24 +348,58 @@ def run_sweep(args):
         prof = upipe.profile_read()
         upipe.profile_enable(False)
         upipe.sync_status()
-        ms = e0.elapsed_time(e1) / args.sweep_steps
+        ms = e0.elapsed_time(e1) / steps
         tf = model_flops_step(sh) / (ms / 1e3) / 1e12
-        print(json.dumps({
+        k_ms = {k: v[0] / steps for k, v in prof.items()}
+        bwd_fl = stb["flops_by_kind"]["attn_bwd"]
+        bwd_tf = bwd_fl / (k_ms["attn_bwd"] / 1e3) / 1e12 if k_ms.get("attn_bwd") else None
+        closed, ulysses = stf["stage_closed_form_bytes"], 12 * sh.S * sh.H * sh.d_head
+        yield {
             "sweep": name, "S": sh.S, "U": sh.U, "C": sh.C, "H": sh.H, "G": sh.G, "d_model": sh.d_model,
-            "schedule": "gqa_out_of_order" if sched else "in_order", "ms_per_step": ms,
-            "tokens_per_s": sh.S / (ms / 1e3), "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops_sustained"],
+            "schedule": "gqa_out_of_order" if sched else "in_order", "steps": steps, "warmup": warmup,
+            "ms_per_step": ms, "tokens_per_s": sh.S / (ms / 1e3), "tflops": tf,
+            "frac_of_bf16_peak": tf / pk["bf16_tflops"],
+            "frac_of_bf16_peak_sustained": tf / pk["bf16_tflops_sustained"],
+            "attn_bwd_tflops": bwd_tf,
+            "attn_bwd_frac": bwd_tf / pk["bf16_tflops"] if bwd_tf else None,
+            "attn_bwd_frac_sustained": bwd_tf / pk["bf16_tflops_sustained"] if bwd_tf else None,
             "stage_arena_fwd_bytes": stf["arena_peak_bytes"], "stage_arena_bwd_bytes": stb["arena_peak_bytes"],
-            "closed_form_12SUd": stf["stage_closed_form_bytes"],
-            "ulysses_form_12SHd": 12 * sh.S * sh.H * sh.d_head,
+            "closed_form_12SUd": closed, "ulysses_form_12SHd": ulysses,
+            "arena_fwd_over_12SUd": stf["arena_peak_bytes"] / closed,
+            "arena_fwd_over_12SHd": stf["arena_peak_bytes"] / ulysses,
+            "arena_bwd_over_12SHd": stb["arena_peak_bytes"] / ulysses,
             "permute_bytes_fwd": stf["permute_bytes"], "permute_bytes_bwd": stb["permute_bytes"],
-            "persistent_bytes": stf["persistent_bytes"], "steps": args.sweep_steps, "clocks": clk,
+            "persistent_bytes": stf["persistent_bytes"], "clocks": clk,
             "workspace_fwd_bytes": wsf.numel(), "workspace_bwd_bytes": wsb.numel(),
             "sequence_chunks": max(n_chunks, 0), "fp8_heads": "all" if n_chunks < 0 else "none",
             "offload_store": where, "offload_bytes": stb["offload_bytes"],
             "offload_copy_bytes": stf["offload_copy_bytes"] + stb["offload_copy_bytes"],
-            "kernel_ms_per_step": {k: v[0] / args.sweep_steps for k, v in prof.items()}}), flush=True)
+            "kernel_ms_per_step": k_ms}
         del X, dY, Wqkv, Wo, wsf, wsb, Y, O, lse, dX, dWqkv, dWo, store, fwd, bwd
         torch.cuda.empty_cache()
+
+
+def with_schedule_ratio(entries):
+    """Adds, to each out-of-order entry with an in-order twin, the ratio of
+    its exchange bytes to the in-order schedule's."""
+    for e in entries:
+        if e["schedule"] != "gqa_out_of_order":
+            continue
+        for f in entries:
+            if f is not e and f["sweep"] == e["sweep"] and f["U"] == e["U"] and f["schedule"] == "in_order":
+                e["permute_bytes_fwd_in_order"] = f["permute_bytes_fwd"]
+                e["permute_bytes_bwd_in_order"] = f["permute_bytes_bwd"]
+                e["permute_fwd_ratio_vs_in_order"] = e["permute_bytes_fwd"] / f["permute_bytes_fwd"]
+    return entries
+
+
+def run_sweep(args):
+    """The other workloads, one JSON line each.  Not the headline."""
+    names = args.sweep_only.split(",") if args.sweep_only else None
+    entries = with_schedule_ratio(list(sweep_entries(sweep_cases(names, extra=True), args.sweep_steps,
+                                                     args.sweep_warmup)))
+    for e in entries:
+        print(json.dumps(e), flush=True)
     return 0
 
 
@@ -371,9 +420,13 @@ def main():
     ap.add_argument("--profile-kernel", default=None, choices=["attn_fwd", "attn_bwd", "all"],
                     help="time one stage's attention kernels alone (no JSON bench line)")
     ap.add_argument("--reps", type=int, default=5)
-    ap.add_argument("--sweep", action="store_true", help="report the other workloads (U sweep, GQA schedule, Qwen)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="only the other workloads, one line each (adds the chunked and FP8 rows)")
     ap.add_argument("--sweep-only", default=None, help="comma-separated workload names for --sweep")
-    ap.add_argument("--sweep-steps", type=int, default=1)
+    ap.add_argument("--sweep-steps", type=int, default=3)
+    ap.add_argument("--sweep-warmup", type=int, default=1)
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="leave the U sweep, Qwen3-32B and 512K rows out of the headline line")
     args = ap.parse_args()
 
     from synthetic import SHAPES
@@ -457,7 +510,10 @@ def main():
     pk = peaks()
     flops_step = model_flops_step(sh)
     tflops = flops_step / (ms_step / 1e3) / 1e12
-    peak_tf = pk["bf16_tflops_sustained"]
+    # the step is timed at full clocks in a sub-second region: the burst
+    # figure is the denominator, the sustained one is reported beside it
+    peak_tf = pk["bf16_tflops"]
+    peak_sus = pk["bf16_tflops_sustained"]
 
     # per-kernel achieved throughput from the live event timings
     kernels = {}
@@ -478,7 +534,8 @@ def main():
         fl_launch = (stf["flops_by_kind"][dom] + stb["flops_by_kind"][dom]) / max(1, kernels[dom]["launches_per_step"])
         achieved = fl_launch / (ms_dom / n_dom / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": achieved / peak_tf, "peak_source": f"{pk['source']} bf16_tflops_sustained",
+                "frac": achieved / peak_tf, "peak_source": f"{pk['source']} bf16_tflops (burst)",
+                "frac_sustained": achieved / peak_sus, "peak_sustained": peak_sus,
                 "flops_per_launch": fl_launch, "ms_per_launch": ms_dom / n_dom,
                 "traffic": measured_traffic(dom, args.workload), "source_sha256_16": source_sha(dom)}
     else:
@@ -564,6 +621,19 @@ def main():
         upipe.sync_status()
 
     mem_peak = torch.cuda.max_memory_allocated(dev) - mem_before
+    # SM clock cycles per step (ms x MHz = thousands of cycles): a step's cost
+    # with the clock taken out
+    if clk.get("sm_mhz"):
+        clk["sm_kcycles_per_step"] = ms_step * clk["sm_mhz"]
+        clk["attn_bwd_sm_kcycles_per_step"] = kernels["attn_bwd"]["ms_per_step"] * clk["sm_mhz"]
+
+    # ---------------- the other workloads (not the headline; outside the timed region) ----------------
+    sweep = None
+    if not args.no_sweep and world == 1:
+        del wsf, wsb
+        torch.cuda.empty_cache()
+        sweep = with_schedule_ratio(list(sweep_entries(sweep_cases(DEFAULT_SWEEP), args.sweep_steps,
+                                                       args.sweep_warmup)))
     if rank != 0:
         return 0
     cpu = None
@@ -577,13 +647,15 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(args, sh),
         "tflops": tflops, "frac_of_bf16_peak": tflops / peak_tf,
-        "peak_source": f"{pk['source']} bf16_tflops_sustained={peak_tf}",
+        "frac_of_bf16_peak_sustained": tflops / peak_sus,
+        "peak_source": f"{pk['source']} bf16_tflops={peak_tf} (burst; sustained {peak_sus} beside)",
         "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": clk,
         "memory": {"stage_arena_bytes": stf["arena_peak_bytes"], "stage_arena_bwd_bytes": stb["arena_peak_bytes"],
                    "closed_form_12SUd": stf["stage_closed_form_bytes"], "persistent_fwd_bytes": stf["persistent_bytes"],
                    "persistent_bwd_bytes": stb["persistent_bytes"], "torch_peak_alloc_bytes": mem_peak,
                    "permute_bytes_per_step": stf["permute_bytes"] + stb["permute_bytes"]},
+        "sweep": sweep,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
