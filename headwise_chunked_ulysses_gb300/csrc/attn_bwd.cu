@@ -18,8 +18,12 @@
 //     columns and into shared memory
 //   dV += P^T dO and dK += dS^T Q (A operands read from TMEM), dQ = dS K
 //     (both operands in shared memory; dQ reuses dP's TMEM columns)
-//   warps 12..15, one query row per thread, move dQ_i out of TMEM and add it
-//     into global memory with fp32 vector reductions.
+//   warps 12..15, one query row per thread, move dQ_i out of TMEM and send
+//     it to the global fp32 accumulator with TMA reduce-adds, staged in the
+//     Q/dO buffer of step i: its dO tile is free once dV_i has run (before
+//     dQ_i), its Q tile once dK_i has; the producer refills that buffer
+//     after the engine has read the staged dQ, so the next dS never waits
+//     for the reduce-adds.
 // MMA issue order dV_i, dQ_i, dK_i, S_{i+1}, dP_{i+1}: dQ_i is drained while
 // dK_i and S_{i+1} run, and dP_{i+1} waits only for dQ_i to have left TMEM.
 // The tensor pipe executes one CTA's MMAs in issue order, so S_{i+1}
@@ -116,13 +120,13 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* s_full = bars + 5;
   uint64_t* dp_full = bars + 6;
   uint64_t* p_ready = bars + 7;
-  uint64_t* dq_staged = bars + 8;  // dQ_i has left the dS tile (TMA reduce mode)
-  uint64_t* ds_ready = bars + 9;
-  uint64_t* ds_consumed = bars + 10;
-  uint64_t* dq_full = bars + 11;
-  uint64_t* dq_drained = bars + 12;
-  uint64_t* kv_done = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* dq_staged = bars + 8;  // [2] per Q/dO stage: its item's dQ has been read out of it (TMA mode)
+  uint64_t* ds_ready = bars + 10;
+  uint64_t* ds_consumed = bars + 11;
+  uint64_t* dq_full = bars + 12;
+  uint64_t* dq_drained = bars + 13;
+  uint64_t* kv_done = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* s_lse = reinterpret_cast<float*>(smem + C::LSE_OFF);
   float* s_D = reinterpret_cast<float*>(smem + C::DS_OFF);
@@ -166,7 +170,8 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(ds_consumed, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_drained, 128);
-    mbar_init(dq_staged, 128);
+    mbar_init(&dq_staged[0], 4);  // lane 0 of each dQ warp
+    mbar_init(&dq_staged[1], 4);
     mbar_init(kv_done, 1);
     *abort_flag = aligned ? 0 : 1;
     if (!aligned && a.status) atomicCAS(a.status, 0, kDevBadSmem);
@@ -201,6 +206,8 @@ __global__ void __launch_bounds__(512, 1)
       for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
         const int st = i & 1;
         if (!mbar_wait(&qdo_empty[st], ((i >> 1) & 1) ^ 1, w, 40)) break;
+        // in the TMA reduce mode the stage's previous item staged its dQ here
+        if (a.dq_tiled == 2 && !mbar_wait(&dq_staged[st], ((i >> 1) & 1) ^ 1, w, 39)) break;
         const long long q_row = static_cast<long long>(cur.qs) * a.S + cur.qb * BQ;
         mbar_arrive_expect_tx(&qdo_full[st], 2 * C::TILE + 2 * BQ * 4);
 #pragma unroll
@@ -357,9 +364,8 @@ __global__ void __launch_bounds__(512, 1)
             pk[(q0 >> 1) + 1] = pack_bf16(f2_lo(db), f2_hi(db));
           }
         }
-        // the dS^T tile is free once the previous step's dQ MMA has read it (and,
-        // when dQ leaves through the TMA engine, once dQ's staging in it is read)
-        if (i > 0 && !mbar_wait_warp(a.dq_tiled == 2 ? dq_staged : ds_consumed, (i - 1) & 1, w, 49)) {
+        // the dS^T tile is free once the previous step's dQ MMA has read it
+        if (i > 0 && !mbar_wait_warp(ds_consumed, (i - 1) & 1, w, 49)) {
           ok = false;
           break;
         }
@@ -418,20 +424,24 @@ __global__ void __launch_bounds__(512, 1)
       cur.seek(a, kvs, item0);
       if (a.dq_tiled == 2) {
         // row-major fp32 dQ through the TMA engine: each warp stages its 32
-        // rows in 32-column chunks (32 x 32 fp32, 128-byte swizzle) in its
-        // 8 KB quarter of the dS tile, two buffers, and issues element-wise
-        // reduce-adds, so the reductions leave the SM without load/store
-        // instructions; the tile is handed back to the softmax warps once
-        // the engine has read the last chunk
+        // rows in 32-column chunks (32 x 32 fp32, 128-byte swizzle, 4 KB)
+        // in its quarter of step i's Q/dO buffer -- the first D/64 chunks in
+        // the dO tile (free: dV_i, its last reader, ran before dQ_i), the
+        // rest in the Q tile once dK_i has completed -- and issues element-
+        // wise reduce-adds; when the engine has read them, the buffer goes
+        // back to the producer
         tma_prefetch_map(&tmDQ);
-        const uint32_t stage = smem_u32(smem + C::DS_TILE_OFF) + (warp & 3) * 8192;
-        int nb = 0;
+        constexpr int NCH = D / 32, HALF = NCH / 2;
+        const uint32_t quarter = (warp & 3) * (C::TILE / 4);
         for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
+          const int st = i & 1;
           if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
           tc_fence_after();
           const int y0 = cur.qs * a.S + cur.qb * BQ + (warp & 3) * 32;
+          const uint32_t s_stage = smem_u32(smem) + st * C::TILE + quarter;
+          bool ok = true;
 #pragma unroll 1
-          for (int c = 0; c < D / 64; ++c) {
+          for (int c = 0; ok && c < D / 64; ++c) {
             uint32_t v[64];
             tmem_ld64(tmem + lane_off + C::T_DP + c * 64, v);
             if (c == D / 64 - 1) {
@@ -440,11 +450,12 @@ __global__ void __launch_bounds__(512, 1)
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const uint32_t buf = stage + (nb & 1) * 4096;
-              if (nb >= 2) {  // the chunk sent two chunks ago has left this buffer
-                if (lane == 0) bulk_wait_read<1>();
-                __syncwarp();
+              const int chunk = 2 * c + h;
+              if (chunk == HALF && !mbar_wait_warp(&qdo_empty[st], (i >> 1) & 1, w, 54)) {
+                ok = false;
+                break;
               }
+              const uint32_t buf = s_stage + (chunk < HALF ? C::DO_OFF : C::Q_OFF) + (chunk % HALF) * 4096;
 #pragma unroll
               for (int p = 0; p < 8; ++p)
                 st_shared_v4(buf + lane * 128 + ((p ^ (lane & 7)) << 4),
@@ -455,15 +466,17 @@ __global__ void __launch_bounds__(512, 1)
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                tma_reduce_add_2d(&tmDQ, buf, c * 64 + h * 32, y0);
+                tma_reduce_add_2d(&tmDQ, buf, chunk * 32, y0);
                 bulk_commit();
               }
-              ++nb;
             }
           }
-          if (lane == 0) bulk_wait_read<0>();
+          if (!ok) break;
+          if (lane == 0) {
+            bulk_wait_read<0>();
+            mbar_arrive(&dq_staged[st]);
+          }
           __syncwarp();
-          mbar_arrive(dq_staged);
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();

@@ -618,6 +618,7 @@ int attention_bwd_enqueue(const void* Q, const void* K, const void* V, const voi
   AttnBwdDesc ab;
   ab.Q = Q; ab.K = K; ab.V = V; ab.dO = dO; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dQ; ab.dK = dK; ab.dV = dV;
   ab.accumulate_kv = 0; ab.S = S; ab.D = d_head; ab.n_qslots = n_q; ab.n_kvslots = n_kv;
+  ab.dq_tiled = 2;  // row-major dQ added by TMA reduce-adds, as in the layer
   for (int k = 0; k < n_q; ++k) ab.kv_slot[k] = static_cast<uint16_t>(kv_of_q[k]);
   return launch_attn_bwd(ab, status, st) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
 }
