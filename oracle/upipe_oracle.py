@@ -799,12 +799,31 @@ def fp8_key_blocks(k):
 def attention_head_forward_fp8(q, k, v):
     """Causal attention whose scores use FP8 Q and K: q = codes * row scale,
     k = codes * block scale, then the exact softmax and P V.  Returns (O, lse)."""
+    qd, kd = fp8_dequantized(q, k)
+    o, lse, _ = attention_head_forward(qd, kd, v)
+    return o, lse
+
+
+def fp8_dequantized(q, k):
+    """The operands the FP8 score path multiplies, as values: q = codes x its
+    row's scale, k = codes x its 128-key block's scale (exact in fp64)."""
     cq, sq = fp8_rows(q)
     ck, sk = fp8_key_blocks(k)
     qd = cq * sq.astype(np.float64)[:, None]
     kd = ck * np.repeat(sk.astype(np.float64), FP8_BLOCK)[:k.shape[0], None]
-    o, lse, _ = attention_head_forward(qd, kd, v)
-    return o, lse
+    return qd, kd
+
+
+def attention_head_backward_fp8(q, k, v, do):
+    """Gradients of <O, dO> for a head attending with FP8 scores
+    (``attention_head_forward_fp8``).  O depends on q and k only through the
+    dequantized operands q~, k~ (``fp8_dequantized``); the attention is
+    differentiated exactly in q~, k~ and v, and the rounding to E4M3, whose
+    derivative is zero almost everywhere, is passed through as the identity
+    (straight-through): dq = dq~, dk = dk~.  Returns (dq, dk, dv)."""
+    qd, kd = fp8_dequantized(q, k)
+    o, _, P = attention_head_forward(qd, kd, v)
+    return attention_head_backward(qd, kd, v, P, o, do)
 
 
 def layer_forward_fp8(X, W_qkv, W_o, H, G, d_head, fp8_heads):
@@ -829,6 +848,46 @@ def layer_forward_fp8(X, W_qkv, W_o, H, G, d_head, fp8_heads):
         O[:, h * d:(h + 1) * d] = o
         lse[h] = l
     return O @ W_o, O, lse
+
+
+def layer_backward_fp8(X, W_qkv, W_o, H, G, d_head, dY, fp8_heads):
+    """``layer_backward`` of ``layer_forward_fp8``: the heads in fp8_heads
+    take their attention gradients from ``attention_head_backward_fp8`` on the
+    bf16-rounded projections (the values their codes are decided from), the
+    others from the plain attention.  The projection gradients then follow as
+    in ``layer_backward``.  Returns (dX, dW_qkv, dW_o)."""
+    S = X.shape[0]
+    d = d_head
+    Wq, Wk, Wv = split_w_qkv(W_qkv, H, G, d)
+    K = [X @ Wk[g] for g in range(G)]
+    V = [X @ Wv[g] for g in range(G)]
+    dK = [np.zeros((S, d)) for _ in range(G)]
+    dV = [np.zeros((S, d)) for _ in range(G)]
+    O = np.zeros((S, H * d))
+    dW_qkv = np.zeros_like(W_qkv)
+    dX = np.zeros_like(X)
+    for h in range(H):
+        g = kv_head(h, H, G)
+        q = X @ Wq[h]
+        do = dY @ W_o[h * d:(h + 1) * d, :].T
+        if h in fp8_heads:
+            qb, kb = bf16_round(q), bf16_round(K[g])
+            qd, kd = fp8_dequantized(qb, kb)
+            o, _, _ = attention_head_forward(qd, kd, V[g])
+            dq, dk, dv = attention_head_backward_fp8(qb, kb, V[g], do)
+        else:
+            o, _, P = attention_head_forward(q, K[g], V[g])
+            dq, dk, dv = attention_head_backward(q, K[g], V[g], P, o, do)
+        O[:, h * d:(h + 1) * d] = o
+        dK[g] += dk
+        dV[g] += dv
+        dW_qkv[:, h * d:(h + 1) * d] = X.T @ dq
+        dX += dq @ Wq[h].T
+    for g in range(G):
+        dW_qkv[:, (H + g) * d:(H + g + 1) * d] = X.T @ dK[g]
+        dW_qkv[:, (H + G + g) * d:(H + G + g + 1) * d] = X.T @ dV[g]
+        dX += dK[g] @ Wk[g].T + dV[g] @ Wv[g].T
+    return dX, dW_qkv, O.T @ dY
 
 
 # ---------------------------------------------------------------------------

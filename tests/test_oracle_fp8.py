@@ -169,3 +169,112 @@ def test_scales_keep_small_and_large_heads_in_range():
 def test_planted_missing_scale_fails_the_pin(monkeypatch):
     monkeypatch.setattr(orc, "fp8_scale", lambda amax: np.float32(1.0))
     assert _scale_gap() > 0.5
+
+
+# ---------------------------------------------------------------------------
+# the backward of FP8-scored heads
+# ---------------------------------------------------------------------------
+
+def _fp8_valued_qk(S=256, d=16, seed=5):
+    """Q rows and K blocks that are E4M3 values times power-of-two scales with
+    their amax at 448 x scale: they quantize to themselves."""
+    rng = np.random.default_rng(seed)
+    v_all = _all_e4m3_values()
+    q = rng.choice(v_all, size=(S, d)) / 8.0
+    k = rng.choice(v_all, size=(S, d)) / 4.0
+    q[:, 0] = 448.0 / 8.0
+    k[::128, 0] = 448.0 / 4.0
+    return q / 64.0 * 8.0, k / 64.0 * 4.0, rng  # scores of moderate size (scales 2^-6, 2^-6)
+
+
+def test_fp8_backward_is_the_exact_backward_on_fp8_inputs():
+    """On inputs the quantizer leaves unchanged, every FP8 gradient is the
+    plain attention gradient of those inputs."""
+    q, k, rng = _fp8_valued_qk()
+    qd, kd = orc.fp8_dequantized(q, k)
+    assert np.array_equal(qd, q) and np.array_equal(kd, k)
+    v = rng.standard_normal(q.shape)
+    do = rng.standard_normal(q.shape)
+    o, _, P = orc.attention_head_forward(q, k, v)
+    want = orc.attention_head_backward(q, k, v, P, o, do)
+    got = orc.attention_head_backward_fp8(q, k, v, do)
+    for a, b in zip(got, want):
+        assert np.abs(a - b).max() <= 1e-12 * np.abs(b).max()
+
+
+def _fp8_backward_fd_gap(seed=6):
+    """Largest gap between the FP8 backward and central differences of
+    L = <O, dO>: in v directly (v is not quantized), and in the dequantized
+    q~, k~ (O is smooth in them) -- the straight-through gradient in q and k is
+    the gradient in q~ and k~.  Sampled entries, two key blocks (the second
+    one short)."""
+    rng = np.random.default_rng(seed)
+    S, d = 130, 4
+    q, k, v, do = (rng.standard_normal((S, d)) for _ in range(4))
+    qd, kd = orc.fp8_dequantized(q, k)
+    dq, dk, dv = orc.attention_head_backward_fp8(q, k, v, do)
+
+    def loss(qq, kk, vv):
+        return float((orc.attention_head_forward(qq, kk, vv)[0] * do).sum())
+
+    eps, worst = 1e-6, 0.0
+    for arr, grad, call in ((v.copy(), dv, lambda a: loss(qd, kd, a)), (qd.copy(), dq, lambda a: loss(a, kd, v)),
+                            (kd.copy(), dk, lambda a: loss(qd, a, v))):
+        for idx in [(i, j) for i in range(0, S, 7) for j in range(d)]:
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = call(arr)
+            arr[idx] = old - eps
+            lm = call(arr)
+            arr[idx] = old
+            worst = max(worst, abs((lp - lm) / (2 * eps) - grad[idx]) / max(1.0, np.abs(grad).max()))
+    return worst
+
+
+def test_fp8_backward_matches_differences_in_the_dequantized_operands():
+    assert _fp8_backward_fd_gap() < 1e-6
+
+
+def test_fp8_layer_backward_without_fp8_heads_is_the_layer_backward():
+    rng = np.random.default_rng(7)
+    S, dm, H, G, d = 128, 16, 4, 2, 8
+    X = rng.standard_normal((S, dm))
+    W_qkv = rng.standard_normal((dm, (H + 2 * G) * d)) / np.sqrt(dm)
+    W_o = rng.standard_normal((H * d, dm)) / np.sqrt(dm)
+    dY = rng.standard_normal((S, dm))
+    want = orc.layer_backward(X, W_qkv, W_o, H, G, d, dY)
+    got = orc.layer_backward_fp8(X, W_qkv, W_o, H, G, d, dY, set())
+    for a, b in zip(got, want):
+        assert np.abs(a - b).max() <= 1e-12 * np.abs(b).max()
+    # with FP8 heads the gradients move by about the format's error, no more
+    got8 = orc.layer_backward_fp8(X, W_qkv, W_o, H, G, d, dY, {0, 3})
+    for a, b in zip(got8, want):
+        gap = np.linalg.norm(a - b) / np.linalg.norm(b)
+        assert 1e-5 < gap < 5e-2
+
+
+def test_planted_unquantized_operand_in_the_fp8_backward_fails(monkeypatch):
+    """A backward that forms dq~ from the unquantized k instead of k~ (a
+    plausible slip) fails the difference pin."""
+    plain_backward = orc.attention_head_backward
+
+    def slipped(q_, k_, v_, do_):
+        qd, kd = orc.fp8_dequantized(q_, k_)
+        o, _, P = orc.attention_head_forward(qd, kd, v_)
+        dq, _, _ = plain_backward(qd, k_, v_, P, o, do_)  # k, not k~
+        _, dk, dv = plain_backward(qd, kd, v_, P, o, do_)
+        return dq, dk, dv
+
+    monkeypatch.setattr(orc, "attention_head_backward_fp8", slipped)
+    assert _fp8_backward_fd_gap() > 1e-3
+
+
+def test_planted_straight_through_on_the_wrong_side_fails(monkeypatch):
+    """Differentiating with the unquantized q and k altogether (no FP8 in the
+    backward at all) fails the pin on FP8-valued inputs' neighbours too."""
+    def slipped(q_, k_, v_, do_):
+        o, _, P = orc.attention_head_forward(q_, k_, v_)
+        return orc.attention_head_backward(q_, k_, v_, P, o, do_)
+
+    monkeypatch.setattr(orc, "attention_head_backward_fp8", slipped)
+    assert _fp8_backward_fd_gap() > 1e-3
