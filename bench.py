@@ -248,15 +248,15 @@ def run_kernel_profile(args, sh):
     return 0
 
 
-DEFAULT_SWEEP = ("llama3_8b_256k_usweep", "qwen3_32b_128k", "llama3_8b_512k_gqa")
+DEFAULT_SWEEP = ("llama3_8b_256k_usweep", "qwen3_32b_128k", "llama3_8b_512k_gqa", "llama3_8b_256k_fp8")
 
 
 def sweep_cases(names=None, extra=False):
     """(workload, shape, schedule, sequence chunks (0: none; -1: FP8 heads),
     offload store) of the other workloads: the U sweep at 256K, the Qwen3-32B
     layer at 128K, the 512K layer under both schedules (the GQA schedule's
-    exchange bytes against the in-order ones); with extra, also the sequence-
-    chunked and FP8 rows."""
+    exchange bytes against the in-order ones), the 256K layer with FP8 heads;
+    with extra, also the sequence-chunked rows and FP8 heads at 32K."""
     from synthetic import SHAPES
     cases = []
     us = SHAPES["llama3_8b_256k_usweep"]
@@ -269,8 +269,10 @@ def sweep_cases(names=None, extra=False):
         # head stages on sequence chunks, K/V offloaded to page-locked host memory
         cases += [("llama3_8b_256k_chunked", us, 0, 8, "host"), ("llama3_8b_256k_chunked", us, 0, 16, "host"),
                   ("llama3_8b_512k_chunked", gq, 0, 16, "host")]
-        # every head's scores in FP8 (forward), bf16 backward
-        cases += [("llama3_8b_32k_fp8", SHAPES["llama3_8b_32k"], 0, -1, None), ("llama3_8b_256k_fp8", us, 0, -1, None)]
+        # every head's scores in FP8, forward and backward
+        cases += [("llama3_8b_32k_fp8", SHAPES["llama3_8b_32k"], 0, -1, None)]
+    # every head's scores in FP8 at 256K: the backward arena against the bf16 row's
+    cases.append(("llama3_8b_256k_fp8", us, 0, -1, None))
     if names:
         cases = [c for c in cases if c[0] in names]
     return cases
@@ -297,15 +299,15 @@ def sweep_entries(cases, steps, warmup):
         Wqkv, Wo = randn(sh.d_model, sh.qkv_cols, std=w_std), randn(sh.H * sh.d_head, sh.d_model, std=w_std)
         store = None
         if n_chunks < 0:
-            wsf = torch.empty(upipe.fwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
-            wsb = torch.empty(upipe.bwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
             all_heads = set(range(sh.H))
+            wsf = torch.empty(upipe.fwd_workspace_bytes(s), dtype=torch.uint8, device=dev)
+            wsb = torch.empty(upipe.bwd_workspace_bytes_fp8(s, all_heads), dtype=torch.uint8, device=dev)
 
             def fwd(**kw):
                 return upipe.attn_fwd_fp8(X, Wqkv, Wo, s, all_heads, ws=wsf, **kw)
 
             def bwd(O, lse, **kw):
-                return upipe.attn_bwd(X, Wqkv, Wo, O, lse, dY, s, ws=wsb, **kw)
+                return upipe.attn_bwd_fp8(X, Wqkv, Wo, O, lse, dY, s, all_heads, ws=wsb, **kw)
         elif n_chunks:
             wsf = torch.empty(upipe.chunked_workspace_bytes(s, n_chunks, False), dtype=torch.uint8, device=dev)
             wsb = torch.empty(upipe.chunked_workspace_bytes(s, n_chunks, True), dtype=torch.uint8, device=dev)

@@ -31,6 +31,7 @@ EXPORTS = (
     "upipe_attn_fwd_chunked", "upipe_attn_bwd_chunked",
     "upipe_quantize_e4m3", "upipe_attention_fwd_fp8", "upipe_attn_fwd_fp8", "upipe_choose_chunks",
     "upipe_layout_head2seq_sum", "upipe_watchdog_selftest",
+    "upipe_attention_bwd_fp8", "upipe_attn_bwd_fp8", "upipe_bwd_workspace_bytes_fp8",
 )
 
 
@@ -90,6 +91,10 @@ def _sig(lib):
         "upipe_quantize_e4m3": (I, [P, I, I, I, LL, I, P, P, P]),
         "upipe_attention_fwd_fp8": (I, [P, P, P, P, P, I, I, I, I, i32p, P, P, P]),
         "upipe_attn_fwd_fp8": (I, [P, P, P] + [I] * 7 + [ctypes.c_char_p, P, P, P, P, Z, P, P]),
+        "upipe_attention_bwd_fp8": (I, [P, P, P, P, P, P, P, P, I, I, I, I, i32p, P, P, P, P, Z, P]),
+        "upipe_attn_bwd_fp8": (I, [P, P, P] + [I] * 7 + [ctypes.c_char_p, P, P, P, P, P, P, P, Z, P,
+                                                          ctypes.POINTER(Stats)]),
+        "upipe_bwd_workspace_bytes_fp8": (Z, [I] * 7 + [ctypes.c_char_p]),
         "upipe_chunked_workspace_bytes": (Z, [I] * 9),
         "upipe_choose_chunks": (I, [I] * 7 + [Z]),
         "upipe_chunked_store_bytes": (Z, [I] * 9),
@@ -291,6 +296,55 @@ def attn_fwd_fp8(X, W_qkv, W_o, sh: Shape, fp8_heads, Y=None, O_saved=None, lse=
         _ptr(Y, bf, "Y"), _ptr(O_saved, bf, "O_saved"), _ptr(lse, f32, "lse"), _ptr(ws), ws.numel(),
         _stream(stream), ctypes.byref(st)))
     return Y, O_saved, lse, st.as_dict()
+
+
+def bwd_workspace_bytes_fp8(sh: Shape, fp8_heads) -> int:
+    """Workspace of attn_bwd_fp8 (smaller when every stage is FP8)."""
+    flags = bytes(1 if h in fp8_heads else 0 for h in range(sh.H))
+    return int(lib().upipe_bwd_workspace_bytes_fp8(*sh.args()[:7], flags))
+
+
+def attn_bwd_fp8(X, W_qkv, W_o, O_saved, lse, dY, sh: Shape, fp8_heads, dX=None, dW_qkv=None, dW_o=None, ws=None,
+                 stream=None):
+    """Layer backward of attn_fwd_fp8 (in-order stages; the flagged stages'
+    attention on the FP8 codes).  Returns (dX, dW_qkv, dW_o, stats)."""
+    torch = _torch()
+    bf, f32 = torch.bfloat16, torch.float32
+    dev = X.device
+    S, dm, H, G, d = sh.S, sh.d_model, sh.H, sh.G, sh.d_head
+    dX = torch.empty(S, dm, dtype=bf, device=dev) if dX is None else dX
+    dW_qkv = torch.empty(dm, (H + 2 * G) * d, dtype=f32, device=dev) if dW_qkv is None else dW_qkv
+    dW_o = torch.empty(H * d, dm, dtype=f32, device=dev) if dW_o is None else dW_o
+    need = bwd_workspace_bytes_fp8(sh, fp8_heads)
+    if need == 0:
+        raise UpipeError("upipe_bwd_workspace_bytes_fp8", EINVAL, "invalid shape")
+    ws = _workspace(need, dev) if ws is None else ws
+    flags = bytes(1 if h in fp8_heads else 0 for h in range(H))
+    st = Stats()
+    _check("upipe_attn_bwd_fp8", lib().upipe_attn_bwd_fp8(
+        _ptr(X, bf, "X"), _ptr(W_qkv, bf, "W_qkv"), _ptr(W_o, bf, "W_o"), *sh.args()[:7], flags,
+        _ptr(O_saved, bf, "O_saved"), _ptr(lse, f32, "lse"), _ptr(dY, bf, "dY"), _ptr(dX, bf, "dX"),
+        _ptr(dW_qkv, f32, "dW_qkv"), _ptr(dW_o, f32, "dW_o"), _ptr(ws), ws.numel(), _stream(stream),
+        ctypes.byref(st)))
+    return dX, dW_qkv, dW_o, st.as_dict()
+
+
+def attention_bwd_fp8(Q8, q_scale, K8, k_scale, V, O, dO, lse, kv_of_q, stream=None):
+    """Backward of attention_fwd_fp8: returns fp32 (dQ, dK, dV), the gradients
+    in the dequantized Q and K."""
+    torch = _torch()
+    bf, f32 = torch.bfloat16, torch.float32
+    n_q, S, d = Q8.shape
+    n_kv = K8.shape[0]
+    dQ = torch.empty(n_q, S, d, dtype=f32, device=Q8.device)
+    dK = torch.empty(n_kv, S, d, dtype=f32, device=Q8.device)
+    dV = torch.empty(n_kv, S, d, dtype=f32, device=Q8.device)
+    ws = torch.empty(8 * n_q * S, dtype=torch.uint8, device=Q8.device)
+    _check("upipe_attention_bwd_fp8", lib().upipe_attention_bwd_fp8(
+        _ptr(Q8, torch.uint8, "Q"), _ptr(q_scale, f32, "q_scale"), _ptr(K8, torch.uint8, "K"),
+        _ptr(k_scale, f32, "k_scale"), _ptr(V, bf, "V"), _ptr(O, bf, "O"), _ptr(dO, bf, "dO"), _ptr(lse, f32, "lse"),
+        n_q, n_kv, S, d, _i32(kv_of_q), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(), _stream(stream)))
+    return dQ, dK, dV
 
 
 def chunked_workspace_bytes(sh: Shape, n_chunks, backward) -> int:

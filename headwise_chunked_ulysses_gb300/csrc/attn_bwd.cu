@@ -8,6 +8,15 @@
 //   dS = P * (dO V^T - rowsum(dO * O))
 //   dQ = dS K / sqrt(d),  dK = sum over those query heads of dS^T Q / sqrt(d)
 //
+// FP8 heads (D = 128): Q and K arrive as E4M3 codes with fp32 scales (Q per
+// row, K per 128-key block), the operands the forward's scores were formed
+// from.  The codes land in the upper half of their bf16 tiles; warps 2 and 3
+// widen them in place -- K's codes exactly (its block scale is a constant of
+// the CTA, folded into the score's exponent factor and into dQ), Q's codes
+// times their row scale, rounded to bf16 -- so the MMAs and the softmax are
+// the bf16 ones.  The gradients in Q and K are those of the dequantized
+// operands (the rounding to E4M3 passed through as the identity).
+//
 // One CTA per (KV slot, 128-row KV block).  It walks every query slot mapped
 // to its KV slot and every query block at or after its KV block, so the GQA
 // reduction of dK/dV happens in TMEM with no atomics.  Per step i:
@@ -56,6 +65,8 @@ struct BwdArgs {
   float* dQacc;
   float* dK;
   float* dV;
+  const float* q_scale;  // FP8 heads: per query row
+  const float* k_scale;  // FP8 heads: per 128-key block, kv_ld / 128 per KV slot
   int* status;
 };
 
@@ -104,9 +115,36 @@ struct ItemCursor {
   }
 };
 
+// E4M3 codes to bf16 in place.  Row r of a 128 x 128 code tile (128-byte
+// swizzled rows, at offset CH of its bf16 tile) becomes row r of the tile's
+// two 64-column bf16 chunks, each value code x scale rounded to bf16 (exact
+// for scale 1).  The row's codes are read before any of its outputs are
+// written, and only row r's bytes are written, so rows convert independently.
+__device__ __forceinline__ void e4m3_row_to_bf16(uint32_t tile, int r, float scale) {
+  const uint32_t sw = static_cast<uint32_t>(r & 7);
+  uint4 c[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) c[u] = ld_shared_v4(tile + CH + r * 128 + ((u ^ sw) << 4));
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {  // codes of columns 16u .. 16u + 15
+    const uint32_t wds[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 a = e4m3x2_to_float2(wds[k] & 0xFFFFu), b = e4m3x2_to_float2(wds[k] >> 16);
+      o[2 * k] = pack_bf16(a.x * scale, a.y * scale);
+      o[2 * k + 1] = pack_bf16(b.x * scale, b.y * scale);
+    }
+    const uint32_t row = tile + (u >> 2) * CH + r * 128;
+    st_shared_v4(row + ((static_cast<uint32_t>((2 * u) & 7) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+    st_shared_v4(row + ((static_cast<uint32_t>((2 * u + 1) & 7) ^ sw) << 4), o[4], o[5], o[6], o[7]);
+  }
+}
+
 // GEN: key offsets, key ranges and split KV blocks (chunk pairs); without it
-// the launch is the plain causal case and those paths compile away.
-template <int D, bool GEN>
+// the launch is the plain causal case and those paths compile away.  F8: Q
+// and K as E4M3 codes (plain launch, D = 128).
+template <int D, bool GEN, bool F8>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -126,7 +164,9 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* dq_full = bars + 12;
   uint64_t* dq_drained = bars + 13;
   uint64_t* kv_done = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* q_ready = bars + 15;   // [2] FP8: the stage's Q codes widened to bf16
+  uint64_t* k_ready = bars + 17;   // FP8: K's codes widened
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* s_lse = reinterpret_cast<float*>(smem + C::LSE_OFF);
   float* s_D = reinterpret_cast<float*>(smem + C::DS_OFF);
@@ -172,6 +212,9 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(dq_drained, 128);
     mbar_init(&dq_staged[0], 4);  // lane 0 of each dQ warp
     mbar_init(&dq_staged[1], 4);
+    mbar_init(&q_ready[0], 64);   // the two converter warps
+    mbar_init(&q_ready[1], 64);
+    mbar_init(k_ready, 64);
     mbar_init(kv_done, 1);
     *abort_flag = aligned ? 0 : 1;
     if (!aligned && a.status) atomicCAS(a.status, 0, kDevBadSmem);
@@ -193,12 +236,13 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmdO);
       const int kv_row = kvs * kv_ld + kvb * BKV;
-      mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+      mbar_arrive_expect_tx(kv_full, (F8 ? CH : C::TILE) + C::TILE);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_2d(smem + C::K_OFF + c * CH, &tmK, kv_full, c * 64, kv_row);
+        if (!F8) tma_load_2d(smem + C::K_OFF + c * CH, &tmK, kv_full, c * 64, kv_row);
         tma_load_2d(smem + C::V_OFF + c * CH, &tmV, kv_full, c * 64, kv_row);
       }
+      if (F8) tma_load_2d(smem + C::K_OFF + CH, &tmK, kv_full, 0, kv_row);  // codes: one 128 x 128 box
       ItemCursor<GEN> cur;
       cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
@@ -209,12 +253,13 @@ __global__ void __launch_bounds__(512, 1)
         // in the TMA reduce mode the stage's previous item staged its dQ here
         if (a.dq_tiled == 2 && !mbar_wait(&dq_staged[st], ((i >> 1) & 1) ^ 1, w, 39)) break;
         const long long q_row = static_cast<long long>(cur.qs) * a.S + cur.qb * BQ;
-        mbar_arrive_expect_tx(&qdo_full[st], 2 * C::TILE + 2 * BQ * 4);
+        mbar_arrive_expect_tx(&qdo_full[st], (F8 ? CH : C::TILE) + C::TILE + 2 * BQ * 4);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_2d(smem + C::Q_OFF + st * C::TILE + c * CH, &tmQ, &qdo_full[st], c * 64, (int)q_row);
+          if (!F8) tma_load_2d(smem + C::Q_OFF + st * C::TILE + c * CH, &tmQ, &qdo_full[st], c * 64, (int)q_row);
           tma_load_2d(smem + C::DO_OFF + st * C::TILE + c * CH, &tmdO, &qdo_full[st], c * 64, (int)q_row);
         }
+        if (F8) tma_load_2d(smem + C::Q_OFF + st * C::TILE + CH, &tmQ, &qdo_full[st], 0, (int)q_row);
         bulk_load(s_lse + st * BQ, a.lse2 + q_row, BQ * 4, &qdo_full[st]);
         bulk_load(s_D + st * BQ, a.Dsum + q_row, BQ * 4, &qdo_full[st]);
       }
@@ -237,7 +282,9 @@ __global__ void __launch_bounds__(512, 1)
           mma_ss(d_tmem, sdesc_advance(a0, off), sdesc_advance(b0, off), ID_S, k > 0);
         }
       };
-      bool ok = mbar_wait(kv_full, 0, w, 41) && mbar_wait(&qdo_full[0], 0, w, 42);
+      // (FP8: the converters' barriers follow the loads' completion)
+      bool ok = F8 ? (mbar_wait(k_ready, 0, w, 41) && mbar_wait(&q_ready[0], 0, w, 42))
+                   : (mbar_wait(kv_full, 0, w, 41) && mbar_wait(&qdo_full[0], 0, w, 42));
       if (ok) {
         tc_fence_after();
         qk_mma(tmem + C::T_S, sK, sQ(0));
@@ -279,7 +326,7 @@ __global__ void __launch_bounds__(512, 1)
         // next S^T: issued after dV_i and dK_i, so it overwrites P^T_i and dS^T_i
         // only once they have been read
         if (i + 1 < n_items) {
-          if (!mbar_wait(&qdo_full[st ^ 1], ((i + 1) >> 1) & 1, w, 44)) break;
+          if (!mbar_wait(F8 ? &q_ready[st ^ 1] : &qdo_full[st ^ 1], ((i + 1) >> 1) & 1, w, 44)) break;
           tc_fence_after();
           qk_mma(tmem + C::T_S, sK, sQ(st ^ 1));
           mma_commit(s_full);
@@ -301,7 +348,8 @@ __global__ void __launch_bounds__(512, 1)
       const int kv_idx = kvb * BKV + row;
       const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
       const uint32_t sDS = smem_u32(smem + C::DS_TILE_OFF);
-      const float sl2 = a.scale_log2;
+      // FP8: K's codes are unscaled; its block scale joins the exponent factor
+      const float sl2 = F8 ? a.scale_log2 * a.k_scale[static_cast<long long>(kvs) * (kv_ld / BKV) + kvb] : a.scale_log2;
       const uint64_t sl2x2 = f2(sl2, sl2);
       ItemCursor<GEN> cur;
       cur.qb_first = qb_first;
@@ -411,6 +459,31 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       }
+    } else if (F8 && (warp == 2 || warp == 3)) {
+      // ---------------- FP8: widen the codes to bf16 in shared memory ----------------
+      // two rows of each 128-row tile per thread: K once, then each item's Q
+      const int t = (warp - 2) * 32 + lane;
+      bool ok = mbar_wait_warp(kv_full, 0, w, 55);
+      if (ok) {
+        e4m3_row_to_bf16(smem_u32(smem + C::K_OFF), t, 1.f);
+        e4m3_row_to_bf16(smem_u32(smem + C::K_OFF), t + 64, 1.f);
+        fence_proxy_async_smem();
+        mbar_arrive(k_ready);
+      }
+      ItemCursor<GEN> cur;
+      cur.qb_first = qb_first;
+      cur.q_blocks = a.q_blocks;
+      cur.seek(a, kvs, item0);
+      for (int i = 0; ok && i < n_items && cur.next(a, kvs); ++i) {
+        const int st = i & 1;
+        if (!mbar_wait_warp(&qdo_full[st], (i >> 1) & 1, w, 56)) break;
+        const float* qsc = a.q_scale + static_cast<long long>(cur.qs) * a.S + cur.qb * BQ;
+        const uint32_t tile = smem_u32(smem + C::Q_OFF + st * C::TILE);
+        e4m3_row_to_bf16(tile, t, qsc[t]);
+        e4m3_row_to_bf16(tile, t + 64, qsc[t + 64]);
+        fence_proxy_async_smem();
+        mbar_arrive(&q_ready[st]);
+      }
     } else if (warp >= 12) {
       // ---------------- dQ: one query row per thread ----------------
       // dQ_i leaves TMEM (freeing dP's columns for dP_{i+1}) and is added into
@@ -418,6 +491,8 @@ __global__ void __launch_bounds__(512, 1)
       // warps' path
       const int row = (warp & 3) * 32 + lane;
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      // dQ = dS K / sqrt(d); FP8: K's block scale as well (K's tile holds its codes)
+      const float dq_mul = F8 ? a.scale * a.k_scale[static_cast<long long>(kvs) * (kv_ld / BKV) + kvb] : a.scale;
       ItemCursor<GEN> cur;
       cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
@@ -459,10 +534,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
               for (int p = 0; p < 8; ++p)
                 st_shared_v4(buf + lane * 128 + ((p ^ (lane & 7)) << 4),
-                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p]) * a.scale),
-                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 1]) * a.scale),
-                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 2]) * a.scale),
-                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 3]) * a.scale));
+                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p]) * dq_mul),
+                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 1]) * dq_mul),
+                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 2]) * dq_mul),
+                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 3]) * dq_mul));
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
@@ -501,9 +576,9 @@ __global__ void __launch_bounds__(512, 1)
             }
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              red_add_v4(col4(c * 16 + e), __uint_as_float(v[4 * e]) * a.scale,
-                         __uint_as_float(v[4 * e + 1]) * a.scale, __uint_as_float(v[4 * e + 2]) * a.scale,
-                         __uint_as_float(v[4 * e + 3]) * a.scale);
+              red_add_v4(col4(c * 16 + e), __uint_as_float(v[4 * e]) * dq_mul,
+                         __uint_as_float(v[4 * e + 1]) * dq_mul, __uint_as_float(v[4 * e + 2]) * dq_mul,
+                         __uint_as_float(v[4 * e + 3]) * dq_mul);
           }
         }
       }
@@ -585,9 +660,9 @@ __global__ void __launch_bounds__(256) dq_tiled_to_seq_kernel(const DqTiledDesc 
   }
 }
 
-template <int D, bool GEN>
+template <int D, bool GEN, bool F8 = false>
 cudaError_t run_bwd(const CUtensorMap* tm, const BwdArgs& args, cudaStream_t st) {
-  auto kern = attn_bwd_kernel<D, GEN>;
+  auto kern = attn_bwd_kernel<D, GEN, F8>;
   // the kernel needs more than the default 48 KB of dynamic shared memory;
   // the limit is raised once per device
   if (const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), BwdCfg<D>::SMEM); e != cudaSuccess)
@@ -627,8 +702,14 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) 
     if (d.kv_slot[i] >= d.n_kvslots) return cudaErrorInvalidValue;
   if (d.dq_tiled < 0 || d.dq_tiled > 2) return cudaErrorInvalidValue;
   CUtensorMap tm[5];
-  if (!make_tmap_bf16(&tm[0], d.Q, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tm[1], d.K, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
+  if (d.fp8 && (d.D != 128 || !d.q_scale || !d.k_scale || d.dq_tiled != 2)) return cudaErrorInvalidValue;
+  if (d.fp8) {  // Q and K codes: one 128 x 128 byte box per tile
+    if (!make_tmap_u8(&tm[0], d.Q, d.D, (uint64_t)d.n_qslots * d.S, d.D, 128, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8(&tm[1], d.K, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 128, 128)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_tmap_bf16(&tm[0], d.Q, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&tm[1], d.K, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
+  }
   if (!make_tmap_bf16(&tm[2], d.V, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tm[3], d.dO, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
   // dQ accumulator as fp32 rows for the TMA reduce mode (otherwise unused)
@@ -662,8 +743,11 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) 
   a.dQacc = d.dQacc;
   a.dK = d.dK;
   a.dV = d.dV;
+  a.q_scale = d.q_scale;
+  a.k_scale = d.k_scale;
   a.status = status;
   const bool gen = d.q_off != 0 || kv_len != d.S || kv_ld != d.S || d.q_split > 1;
+  if (d.fp8) return gen ? cudaErrorInvalidValue : run_bwd<128, false, true>(tm, a, st);
   if (gen) return d.D == 128 ? run_bwd<128, true>(tm, a, st) : run_bwd<64, true>(tm, a, st);
   return d.D == 128 ? run_bwd<128, false>(tm, a, st) : run_bwd<64, false>(tm, a, st);
 }

@@ -260,10 +260,40 @@ void build_schedule(Plan& p) {
   if (s.sched == UPIPE_SCHED_GQA_OOO) p.max_cols = std::max(p.max_cols, 2 * s.G);
 }
 
+// FP8 stage buffers inside the head-layout region of a stage: Q and K as E4M3
+// codes, V in bf16, the fp32 scales of Q rows and of 128-key blocks of K
+struct Fp8Stage {
+  uint8_t* q = nullptr;
+  uint8_t* k = nullptr;
+  uint16_t* v = nullptr;
+  float* qs = nullptr;
+  float* ks = nullptr;
+  size_t bytes = 0;
+};
+
+Fp8Stage fp8_stage_buffers(const Plan& p, uint8_t* base) {
+  const Shape& s = p.sh;
+  const size_t Sd = static_cast<size_t>(s.S) * s.d;
+  Fp8Stage f;
+  const size_t o_k = align256(s.U * Sd);
+  const size_t o_v = align256(o_k + p.n_kv_slots * Sd);
+  const size_t o_qs = align256(o_v + p.n_kv_slots * Sd * 2);
+  const size_t o_ks = align256(o_qs + static_cast<size_t>(s.U) * s.S * 4);
+  f.bytes = o_ks + static_cast<size_t>(p.n_kv_slots) * (s.S / 128) * 4;
+  if (base) {
+    f.q = base;
+    f.k = base + o_k;
+    f.v = reinterpret_cast<uint16_t*>(base + o_v);
+    f.qs = reinterpret_cast<float*>(base + o_qs);
+    f.ks = reinterpret_cast<float*>(base + o_ks);
+  }
+  return f;
+}
+
 // Workspace: [stage arena | persistent].  The stage arena holds the sequence-
 // layout stage buffer (QKV, then reused for dO and dQKV) and the head-layout
 // exchange buffers; the persistent part holds the fp32 Y / dX accumulator.
-Plan make_plan(const Shape& s, bool backward, bool prefetch = false) {
+Plan make_plan(const Shape& s, bool backward, bool prefetch = false, bool fp8_all = false) {
   Plan p;
   p.sh = s;
   build_schedule(p);
@@ -272,7 +302,9 @@ Plan make_plan(const Shape& s, bool backward, bool prefetch = false) {
   p.off_seq = o;
   o = align256(o + S * p.max_cols * d * 2);
   p.off_qkvh = o;
-  o = align256(o + (U + 2 * p.n_kv_slots) * S * d * 2);
+  // head-layout stage buffers; when every stage runs FP8 scores they hold Q
+  // and K codes with their scales and bf16 V (fp8_all: backward plans only)
+  o = align256(o + (fp8_all ? fp8_stage_buffers(p, nullptr).bytes : (U + 2 * p.n_kv_slots) * S * d * 2));
   if (backward) {
     p.off_doh = o;
     o = align256(o + U * S * d * 2);
@@ -300,6 +332,14 @@ Plan make_plan(const Shape& s, bool backward, bool prefetch = false) {
   p.persistent = o - p.arena;
   p.total = o;
   return p;
+}
+
+// Whether every stage of the plan is flagged FP8 (in-order stages).
+bool all_stages_fp8(const Plan& p, const uint8_t* fp8_heads) {
+  if (!fp8_heads) return false;
+  for (const Stage& g : p.st)
+    if (!fp8_heads[g.q_heads[0]]) return false;
+  return true;
 }
 
 // Split of a long-K contraction so that its output tiles fill the GPU: the
@@ -457,36 +497,6 @@ struct Launcher {
     run(UPIPE_KERNEL_BWD_PREP, 0.0, b, [&] { return launch_bwd_prep(p, st); });
   }
 };
-
-// FP8 stage buffers inside the head-layout region of a stage: Q and K as E4M3
-// codes, V in bf16, the fp32 scales of Q rows and of 128-key blocks of K
-struct Fp8Stage {
-  uint8_t* q = nullptr;
-  uint8_t* k = nullptr;
-  uint16_t* v = nullptr;
-  float* qs = nullptr;
-  float* ks = nullptr;
-  size_t bytes = 0;
-};
-
-Fp8Stage fp8_stage_buffers(const Plan& p, uint8_t* base) {
-  const Shape& s = p.sh;
-  const size_t Sd = static_cast<size_t>(s.S) * s.d;
-  Fp8Stage f;
-  const size_t o_k = align256(s.U * Sd);
-  const size_t o_v = align256(o_k + p.n_kv_slots * Sd);
-  const size_t o_qs = align256(o_v + p.n_kv_slots * Sd * 2);
-  const size_t o_ks = align256(o_qs + static_cast<size_t>(s.U) * s.S * 4);
-  f.bytes = o_ks + static_cast<size_t>(p.n_kv_slots) * (s.S / 128) * 4;
-  if (base) {
-    f.q = base;
-    f.k = base + o_k;
-    f.v = reinterpret_cast<uint16_t*>(base + o_v);
-    f.qs = reinterpret_cast<float*>(base + o_qs);
-    f.ks = reinterpret_cast<float*>(base + o_ks);
-  }
-  return f;
-}
 
 // The exchange of an FP8 stage from the projected sequence buffer: Q rows and
 // K blocks encoded with their scales, V moved as bf16.
@@ -647,6 +657,14 @@ size_t upipe_bwd_workspace_bytes(int S, int d_model, int H, int G, int d_head, i
   return make_plan(s, true).total;
 }
 
+size_t upipe_bwd_workspace_bytes_fp8(int S, int d_model, int H, int G, int d_head, int U, int C,
+                                     const uint8_t* fp8_heads) {
+  const Shape s{S, d_model, H, G, d_head, U, C, UPIPE_SCHED_INORDER};
+  if (check_shape(s) != UPIPE_OK || !fp8_heads) return 0;
+  const Plan p = make_plan(s, true);
+  return all_stages_fp8(p, fp8_heads) ? make_plan(s, true, false, true).total : p.total;
+}
+
 }  // extern "C"
 
 namespace {
@@ -772,10 +790,11 @@ int attn_fwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
 int attn_bwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model, int H,
                    int G, int d_head, int U, int C, int sched, const upipe_bf16* O_saved, const float* lse,
                    const upipe_bf16* dY, upipe_bf16* dX, float* dW_qkv, float* dW_o, void* ws, size_t ws_bytes,
-                   void* stream, upipe_stats* stats) {
+                   void* stream, upipe_stats* stats, const uint8_t* fp8_heads = nullptr) {
   const Shape s{S, d_model, H, G, d_head, U, C, sched};
   if (check_shape(s) != UPIPE_OK) return check_shape(s);
-  const Plan p = make_plan(s, true);
+  const Plan p0 = make_plan(s, true);
+  const Plan p = all_stages_fp8(p0, fp8_heads) ? make_plan(s, true, false, true) : p0;
   const void* ptrs[] = {X, W_qkv, W_o, O_saved, lse, dY, dX, dW_qkv, dW_o};
   int rc = common_checks(s, ptrs, 9, ws, ws_bytes, p.total);
   if (rc != UPIPE_OK) return rc;
@@ -829,8 +848,10 @@ int attn_bwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
 
   for (int i = 0; i < p.n_stages && L.ok(); ++i) {
     const Stage& g = p.st[i];
-    // recompute (1) and (2)
-    project_and_exchange(L, p, i, X, W_qkv, w);
+    // recompute (1) and (2); an FP8 stage exchanges Q and K as the codes its
+    // forward attended with
+    const bool f8 = fp8_heads && fp8_heads[g.q_heads[0]];
+    project_and_exchange(L, p, i, X, W_qkv, w, 0, f8);
     // dO_s = dY W_o[rows of the stage]^T in sequence layout (the QKV sequence buffer is dead)
     GemmDesc gd;
     gd.A = dY; gd.lda = d_model; gd.a_rows = S; gd.a_cols = d_model; gd.a_mn = false;
@@ -862,6 +883,11 @@ int attn_bwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
     ab.Q = qkvh;
     ab.K = qkvh + U * slot_elems;
     ab.V = qkvh + (U + p.n_kv_slots) * slot_elems;
+    if (f8) {
+      const Fp8Stage f = fp8_stage_buffers(p, reinterpret_cast<uint8_t*>(qkvh));
+      ab.Q = f.q; ab.K = f.k; ab.V = f.v;
+      ab.fp8 = true; ab.q_scale = f.qs; ab.k_scale = f.ks;
+    }
     ab.dO = doh; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dacc;
     ab.dK = dacc + U * slot_elems;
     ab.dV = dacc + (U + p.n_kv_slots) * slot_elems;
@@ -1203,6 +1229,65 @@ int upipe_attn_fwd_fp8(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe
   }
   return attn_fwd_issue(X, W_qkv, W_o, S, d_model, H, G, d_head, U, C, UPIPE_SCHED_INORDER, Y, O_saved, lse, ws,
                         ws_bytes, stream, stats, false, any ? fp8_heads : nullptr);
+}
+
+int upipe_attn_bwd_fp8(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model,
+                       int H, int G, int d_head, int U, int C, const uint8_t* fp8_heads, const upipe_bf16* O_saved,
+                       const float* lse, const upipe_bf16* dY, upipe_bf16* dX, float* dW_qkv, float* dW_o, void* ws,
+                       size_t ws_bytes, void* stream, upipe_stats* stats) {
+  const Shape s{S, d_model, H, G, d_head, U, C, UPIPE_SCHED_INORDER};
+  int rc = check_shape(s);
+  if (rc != UPIPE_OK) return rc;
+  if (!fp8_heads) return UPIPE_EINVAL;
+  const Plan p = make_plan(s, true);
+  bool any = false;
+  for (const Stage& g : p.st) {
+    const uint8_t f = fp8_heads[g.q_heads[0]] ? 1 : 0;
+    for (int h : g.q_heads)
+      if ((fp8_heads[h] ? 1 : 0) != f) return UPIPE_EINVAL;  // a stage runs in one precision
+    any = any || f;
+  }
+  if (any) {
+    if (d_head != 128) return UPIPE_EUNSUPPORTED;
+    const size_t region = static_cast<size_t>(U + 2 * p.n_kv_slots) * S * d_head * 2;
+    if (fp8_stage_buffers(p, nullptr).bytes > region) return UPIPE_EUNSUPPORTED;
+  }
+  return attn_bwd_issue(X, W_qkv, W_o, S, d_model, H, G, d_head, U, C, UPIPE_SCHED_INORDER, O_saved, lse, dY, dX,
+                        dW_qkv, dW_o, ws, ws_bytes, stream, stats, any ? fp8_heads : nullptr);
+}
+
+int upipe_attention_bwd_fp8(const uint8_t* Q, const float* q_scale, const uint8_t* K, const float* k_scale,
+                            const upipe_bf16* V, const upipe_bf16* O, const upipe_bf16* dO, const float* lse, int n_q,
+                            int n_kv, int S, int d_head, const int32_t* kv_of_q, float* dQ, float* dK, float* dV,
+                            void* ws, size_t ws_bytes, void* stream) {
+  if (!q_scale || !k_scale || !aligned16(q_scale) || !aligned16(k_scale)) return UPIPE_EINVAL;
+  const int rc = attention_bwd_check(Q, K, V, O, dO, lse, n_q, n_kv, S, d_head, kv_of_q, dQ, dK, dV);
+  if (rc != UPIPE_OK) return rc;
+  if (d_head != 128) return UPIPE_EUNSUPPORTED;
+  if (!ws || !aligned16(ws)) return UPIPE_EINVAL;
+  if (ws_bytes < attention_bwd_scratch_bytes(n_q, S)) return UPIPE_ENOSPC;
+  if (!device_supported()) return UPIPE_EUNSUPPORTED;
+  int* status = status_ptr();
+  if (!status) return UPIPE_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* dsum = static_cast<float*>(ws);
+  float* lse2 = dsum + static_cast<size_t>(n_q) * S;
+  BwdPrepDesc pr;
+  pr.dO = dO; pr.ld_do = d_head; pr.O = O; pr.ld_o = d_head; pr.lse = lse;
+  pr.Dsum = dsum; pr.lse2 = lse2; pr.dQacc = dQ; pr.S = S; pr.D = d_head; pr.n_slots = n_q;
+  for (int k = 0; k < n_q; ++k) {
+    pr.do_unit[k] = k * S;
+    pr.o_unit[k] = k * S;
+    pr.lse_row[k] = static_cast<uint16_t>(k);
+  }
+  if (launch_bwd_prep(pr, st) != cudaSuccess) return UPIPE_ECUDA;
+  AttnBwdDesc ab;
+  ab.Q = Q; ab.K = K; ab.V = V; ab.dO = dO; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dQ; ab.dK = dK; ab.dV = dV;
+  ab.accumulate_kv = 0; ab.S = S; ab.D = d_head; ab.n_qslots = n_q; ab.n_kvslots = n_kv;
+  ab.dq_tiled = 2;
+  ab.fp8 = true; ab.q_scale = q_scale; ab.k_scale = k_scale;
+  for (int k = 0; k < n_q; ++k) ab.kv_slot[k] = static_cast<uint16_t>(kv_of_q[k]);
+  return launch_attn_bwd(ab, status, st) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
 }
 
 int upipe_attention_bwd(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf16* V, const upipe_bf16* O,

@@ -95,6 +95,11 @@ struct AttnBwdDesc {
   // into buffers that hold zeros or earlier partial sums (accumulate_kv is
   // then implied and nothing is zero-filled)
   int q_split = 1;
+  // FP8 heads (plain launch, D = 128, dq_tiled = 2): Q and K hold E4M3 codes,
+  // one byte each, with q_scale [n_qslots][S] and k_scale [n_kvslots][kv_ld / 128]
+  bool fp8 = false;
+  const float* q_scale = nullptr;
+  const float* k_scale = nullptr;
   uint16_t kv_slot[kMaxSlots];  // q slot -> kv slot
 };
 

@@ -316,12 +316,51 @@ int upipe_attention_fwd_fp8(const uint8_t* Q, const float* q_scale, const uint8_
  * buffers take (U + n_kv) S d_head bytes of codes plus 2 n_kv S d_head of V
  * where the bf16 stage takes 2 (U + 2 n_kv) S d_head.  FP8 stages need
  * d_head = 128 (UPIPE_EUNSUPPORTED otherwise).  O_saved and lse feed
- * upipe_attn_bwd as usual; that backward recomputes in bf16, so its gradients
- * are those of the bf16 layer at the FP8 forward's softmax statistics.
+ * upipe_attn_bwd_fp8 (the exact backward of this forward) or upipe_attn_bwd
+ * (which recomputes the scores in bf16: the gradients of the bf16 layer at the
+ * FP8 forward's softmax statistics).
  */
 int upipe_attn_fwd_fp8(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model,
                        int H, int G, int d_head, int U, int C, const uint8_t* fp8_heads, upipe_bf16* Y,
                        upipe_bf16* O_saved, float* lse, void* ws, size_t ws_bytes, void* stream, upipe_stats* stats);
+
+/*
+ * The backward of upipe_attention_fwd_fp8 (the pages give no backward; this
+ * is the exact gradient of the FP8-scored attention in its dequantized
+ * operands, the rounding to E4M3 passed through as the identity): the scores
+ * are recomputed from the same codes and scales the forward used, dV = P^T dO,
+ * dS = P * (dO V^T - rowsum(dO * O)), dQ = dS K~ / sqrt(d), dK = dS^T Q~ /
+ * sqrt(d), with K~ = codes x block scale and Q~ = codes x row scale (Q~ is
+ * rounded to bf16 on the way to the tensor cores).  Q, q_scale, K, k_scale as
+ * for upipe_attention_fwd_fp8; V, O, dO, lse, outputs, workspace and errors as
+ * for upipe_attention_bwd.  d_head 128 only.
+ */
+int upipe_attention_bwd_fp8(const uint8_t* Q, const float* q_scale, const uint8_t* K, const float* k_scale,
+                            const upipe_bf16* V, const upipe_bf16* O, const upipe_bf16* dO, const float* lse, int n_q,
+                            int n_kv, int S, int d_head, const int32_t* kv_of_q, float* dQ, float* dK, float* dV,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The layer backward (in-order schedule) of upipe_attn_fwd_fp8: the stages
+ * whose heads are flagged in fp8_heads (HOST, H bytes, the same flags as the
+ * forward) recompute their projection, exchange Q and K as E4M3 codes with
+ * their scales (the operands the forward attended with) and run the FP8
+ * attention backward above; other stages are as in upipe_attn_bwd.
+ * Gradients in X and the weights follow through the dequantized Q and K.
+ * Workspace: upipe_bwd_workspace_bytes_fp8() bytes -- when every stage is
+ * FP8, the head-layout stage buffers hold (U + n_kv) S d_head bytes of codes,
+ * 2 n_kv S d_head of V and the scales instead of 2 (U + 2 n_kv) S d_head, and
+ * the arena (stats->arena_peak_bytes) is that much smaller; otherwise it is
+ * upipe_bwd_workspace_bytes() of the in-order schedule.  FP8 stages need
+ * d_head = 128 (UPIPE_EUNSUPPORTED otherwise); a stage whose heads carry
+ * different flags is UPIPE_EINVAL.
+ */
+size_t upipe_bwd_workspace_bytes_fp8(int S, int d_model, int H, int G, int d_head, int U, int C,
+                                     const uint8_t* fp8_heads);
+int upipe_attn_bwd_fp8(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf16* W_o, int S, int d_model,
+                       int H, int G, int d_head, int U, int C, const uint8_t* fp8_heads, const upipe_bf16* O_saved,
+                       const float* lse, const upipe_bf16* dY, upipe_bf16* dX, float* dW_qkv, float* dW_o, void* ws,
+                       size_t ws_bytes, void* stream, upipe_stats* stats);
 
 /*
  * Its backward pass.  dO: device bf16 [n_q][S][d_head]; O, lse from the forward.

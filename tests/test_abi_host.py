@@ -332,3 +332,21 @@ def test_library_accepts_exactly_the_method_shapes_within_its_tiling(upipe):
             seen_bad += 1
     assert seen_ok > 100 and seen_bad > 100
     assert alone["3U"] > 0 and alone["cols"] > 0 and alone["U+2kv"] == 0 and broken_kv > 0, (alone, broken_kv)
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_32k", "qwen3_32b_128k", "llama3_8b_256k_usweep"])
+def test_fp8_backward_workspace_keeps_codes(upipe, name):
+    """With every stage FP8 the backward's head-layout stage buffers hold Q and
+    K as one-byte codes (U query slots, U per-slot K copies in order) plus
+    their fp32 scales, and bf16 V: 2 U S d fewer bytes than the bf16 plan, less
+    the scales (4 U S for Q rows, 4 U S / 128 for K blocks) and alignment.
+    A stage left in bf16 keeps the bf16 plan."""
+    from synthetic import SHAPES
+    s = SHAPES[name]
+    sh = upipe.Shape(s.S, s.d_model, s.H, s.G, s.d_head, s.U, s.C, upipe.IN_ORDER)
+    plain = upipe.bwd_workspace_bytes(sh)
+    every = upipe.bwd_workspace_bytes_fp8(sh, set(range(s.H)))
+    saved = 2 * s.U * s.S * s.d_head - 4 * s.U * s.S - 4 * s.U * (s.S // 128)
+    assert 0 <= (plain - every) - saved <= 4 * 256
+    assert upipe.bwd_workspace_bytes_fp8(sh, set(range(s.U))) == plain  # the first stage only
+    assert upipe.bwd_workspace_bytes_fp8(sh, set()) == plain

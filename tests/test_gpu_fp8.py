@@ -148,3 +148,83 @@ def test_fp8_argument_errors(up):
     with pytest.raises(up.UpipeError) as e:
         up.attn_fwd_fp8(td["X"], td["W_qkv"], td["W_o"], ts, {0, 1})
     assert e.value.code == up.EUNSUPPORTED
+
+
+# ---------------------------------------------------------------------------
+# the FP8 backward: the exact gradient of the FP8-scored attention in its
+# dequantized operands (straight-through for the rounding), as the oracle's
+# attention_head_backward_fp8 / layer_backward_fp8 define it
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n_q,n_kv,S,kv", [(4, 2, 1024, [0, 0, 1, 1]), (2, 2, 384, [1, 0]), (3, 1, 256, [0, 0, 0])])
+def test_fp8_attention_backward_matches_the_oracle(up, n_q, n_kv, S, kv):
+    import torch
+    d = 128
+    Qb = normal_bf16((S, n_q * d), 21)
+    Kb = normal_bf16((S, n_kv * d), 22)
+    Vb = normal_bf16((n_kv, S, d), 23)
+    dOb = normal_bf16((n_q, S, d), 24)
+    q8, qs = up.quantize_e4m3(to_dev(Qb), S, n_q, d, n_q * d, True)
+    k8, ks = up.quantize_e4m3(to_dev(Kb), S, n_kv, d, n_kv * d, False)
+    V, dO = to_dev(Vb), to_dev(dOb)
+    O, lse = up.attention_fwd_fp8(q8, qs, k8, ks, V, kv)
+    dQ, dK, dV = up.attention_bwd_fp8(q8, qs, k8, ks, V, O, dO, lse, kv)
+    torch.cuda.synchronize()
+    up.sync_status()
+    q64, k64, v64, do64 = (bf16_bits_to_f64(x) for x in (Qb, Kb, Vb, dOb))
+    dK_ref, dV_ref = np.zeros((n_kv, S, d)), np.zeros((n_kv, S, d))
+    for h in range(n_q):
+        g = kv[h]
+        dq, dk, dv = orc.attention_head_backward_fp8(q64[:, h * d:(h + 1) * d], k64[:, g * d:(g + 1) * d], v64[g],
+                                                     do64[h])
+        assert rel(f64_of(dQ[h]), dq) <= TOL, ("dQ", h)
+        dK_ref[g] += dk
+        dV_ref[g] += dv
+    for g in range(n_kv):
+        assert rel(f64_of(dK[g]), dK_ref[g]) <= TOL, ("dK", g)
+        assert rel(f64_of(dV[g]), dV_ref[g]) <= TOL, ("dV", g)
+
+
+@pytest.mark.parametrize("fp8_heads", [{0, 1}, {2, 3}, {0, 1, 2, 3}])
+def test_layer_backward_with_fp8_stages(up, fp8_heads):
+    """The layer backward of FP8 stages against the oracle's FP8 layer
+    backward; with every stage FP8 the backward arena shrinks by the codes."""
+    import torch
+    sh = TINY128
+    bits = layer_inputs(sh, 0)
+    d = {k: to_dev(v) for k, v in bits.items()}
+    f = {k: bf16_bits_to_f64(v) for k, v in bits.items()}
+    s = up.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, sh.U, sh.C, 0)
+    Y, O, lse, _ = up.attn_fwd_fp8(d["X"], d["W_qkv"], d["W_o"], s, fp8_heads)
+    dX, dWq, dWo, stb = up.attn_bwd_fp8(d["X"], d["W_qkv"], d["W_o"], O, lse, d["dY"], s, fp8_heads)
+    torch.cuda.synchronize()
+    up.sync_status()
+    want = orc.layer_backward_fp8(f["X"], f["W_qkv"], f["W_o"], sh.H, sh.G, sh.d_head, f["dY"], fp8_heads)
+    for name, a, b in zip(("dX", "dW_qkv", "dW_o"), (dX, dWq, dWo), want):
+        assert rel(f64_of(a), b) <= TOL, name
+    plain = up.bwd_workspace_bytes(s)
+    fp8 = up.bwd_workspace_bytes_fp8(s, fp8_heads)
+    if len(fp8_heads) == sh.H:
+        slot = sh.S * sh.d_head
+        assert plain - fp8 >= 2 * sh.U * slot - 8 * sh.U * sh.S - 1024  # Q, K codes: 1 byte instead of 2
+    else:
+        assert fp8 == plain
+
+
+def test_llama_widths_4k_all_fp8_backward(up):
+    import torch
+    sh = SHAPES["llama3_8b_4k"]
+    bits = layer_inputs(sh, 0)
+    d = {k: to_dev(v) for k, v in bits.items()}
+    s = up.Shape(sh.S, sh.d_model, sh.H, sh.G, sh.d_head, sh.U, sh.C, 0)
+    heads = set(range(sh.H))
+    Y, O, lse, _ = up.attn_fwd_fp8(d["X"], d["W_qkv"], d["W_o"], s, heads)
+    dX, dWq, dWo, stb = up.attn_bwd_fp8(d["X"], d["W_qkv"], d["W_o"], O, lse, d["dY"], s, heads)
+    torch.cuda.synchronize()
+    up.sync_status()
+    f = {k: bf16_bits_to_f64(v) for k, v in bits.items()}
+    want = orc.layer_backward_fp8(f["X"], f["W_qkv"], f["W_o"], sh.H, sh.G, sh.d_head, f["dY"], heads)
+    for name, a, b in zip(("dX", "dW_qkv", "dW_o"), (dX, dWq, dWo), want):
+        assert rel(f64_of(a), b) <= TOL, name
+    _, _, _, stp = up.attn_bwd(d["X"], d["W_qkv"], d["W_o"], O, lse, d["dY"], s)
+    assert stb["arena_peak_bytes"] < stp["arena_peak_bytes"]
