@@ -10,11 +10,13 @@
 //
 // FP8 heads (D = 128): Q and K arrive as E4M3 codes with fp32 scales (Q per
 // row, K per 128-key block), the operands the forward's scores were formed
-// from.  The codes land in the upper half of their bf16 tiles; warps 2 and 3
-// widen them in place -- K's codes exactly (its block scale is a constant of
-// the CTA, folded into the score's exponent factor and into dQ), Q's codes
-// times their row scale, rounded to bf16 -- so the MMAs and the softmax are
-// the bf16 ones.  The gradients in Q and K are those of the dequantized
+// from.  The codes land in the upper half of their bf16 tiles and are widened
+// in place on the integer and FMA pipes (the special-function pipe is the
+// softmax's): K's codes once, exactly, by warps 2 and 3 (its block scale is a
+// constant of the CTA, folded into the score's exponent factor and into dQ);
+// each item's Q codes times their row scale, rounded to bf16, by the first-
+// half softmax warps in their idle time after the previous item's dS -- so the
+// MMAs and the softmax are the bf16 ones.  The gradients in Q and K are those of the dequantized
 // operands (the rounding to E4M3 passed through as the identity).
 //
 // One CTA per (KV slot, 128-row KV block).  It walks every query slot mapped
@@ -130,10 +132,11 @@ __device__ __forceinline__ void e4m3_row_to_bf16(uint32_t tile, int r, float sca
     const uint32_t wds[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
     uint32_t o[8];
 #pragma unroll
+    const uint64_t sc = f2(scale, scale);
     for (int k = 0; k < 4; ++k) {
-      const float2 a = e4m3x2_to_float2(wds[k] & 0xFFFFu), b = e4m3x2_to_float2(wds[k] >> 16);
-      o[2 * k] = pack_bf16(a.x * scale, a.y * scale);
-      o[2 * k + 1] = pack_bf16(b.x * scale, b.y * scale);
+      const uint64_t a = mul2(e4m3x2_to_f2(wds[k] & 0xFFFFu), sc), b = mul2(e4m3x2_to_f2(wds[k] >> 16), sc);
+      o[2 * k] = pack_bf16(f2_lo(a), f2_hi(a));
+      o[2 * k + 1] = pack_bf16(f2_lo(b), f2_hi(b));
     }
     const uint32_t row = tile + (u >> 2) * CH + r * 128;
     st_shared_v4(row + ((static_cast<uint32_t>((2 * u) & 7) ^ sw) << 4), o[0], o[1], o[2], o[3]);
@@ -164,7 +167,7 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* dq_full = bars + 12;
   uint64_t* dq_drained = bars + 13;
   uint64_t* kv_done = bars + 14;
-  uint64_t* q_ready = bars + 15;   // [2] FP8: the stage's Q codes widened to bf16
+  uint64_t* q_ready = bars + 15;   // [2] FP8: the stage's Q codes widened (first-half softmax warps)
   uint64_t* k_ready = bars + 17;   // FP8: K's codes widened
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -212,9 +215,9 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(dq_drained, 128);
     mbar_init(&dq_staged[0], 4);  // lane 0 of each dQ warp
     mbar_init(&dq_staged[1], 4);
-    mbar_init(&q_ready[0], 64);   // the two converter warps
-    mbar_init(&q_ready[1], 64);
-    mbar_init(k_ready, 64);
+    mbar_init(&q_ready[0], 128);  // the four first-half softmax warps
+    mbar_init(&q_ready[1], 128);
+    mbar_init(k_ready, 64);       // warps 2 and 3
     mbar_init(kv_done, 1);
     *abort_flag = aligned ? 0 : 1;
     if (!aligned && a.status) atomicCAS(a.status, 0, kDevBadSmem);
@@ -356,8 +359,21 @@ __global__ void __launch_bounds__(512, 1)
       cur.q_blocks = a.q_blocks;
       cur.seek(a, kvs, item0);
       bool ok = true;
+      // FP8: the first-half warps widen each item's Q codes (a row per
+      // thread), item 0 here and item i+1 after dS_i, one item ahead of its S^T
+      ItemCursor<GEN> ahead = cur;
+      auto widen_q = [&](int j) -> bool {
+        if (!ahead.next(a, kvs)) return true;
+        if (!mbar_wait_warp(&qdo_full[j & 1], (j >> 1) & 1, w, 56)) return false;
+        const float qs = a.q_scale[static_cast<long long>(ahead.qs) * a.S + ahead.qb * BQ + row];
+        e4m3_row_to_bf16(smem_u32(smem + C::Q_OFF + (j & 1) * C::TILE), row, qs);
+        fence_proxy_async_smem();
+        mbar_arrive(&q_ready[j & 1]);
+        return true;
+      };
+      if (F8 && half == 0 && n_items > 0) ok = widen_q(0);
       int i = 0;
-      for (; i < n_items && cur.next(a, kvs); ++i) {
+      for (; ok && i < n_items && cur.next(a, kvs); ++i) {
         const int st = i & 1;
         const bool diag = (cur.qb + q_off_blocks == kvb);
         if (!mbar_wait_warp(s_full, i & 1, w, 47)) { ok = false; break; }
@@ -427,6 +443,10 @@ __global__ void __launch_bounds__(512, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(ds_ready);
+        if (F8 && half == 0 && i + 1 < n_items && !widen_q(i + 1)) {
+          ok = false;
+          break;
+        }
       }
       // dK, dV epilogue: this thread's half of the d columns of KV row `row`
       if (ok && mbar_wait_warp(kv_done, 0, w, 52)) {
@@ -460,29 +480,13 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
     } else if (F8 && (warp == 2 || warp == 3)) {
-      // ---------------- FP8: widen the codes to bf16 in shared memory ----------------
-      // two rows of each 128-row tile per thread: K once, then each item's Q
+      // ---------------- FP8: widen K's codes to bf16, once ----------------
       const int t = (warp - 2) * 32 + lane;
-      bool ok = mbar_wait_warp(kv_full, 0, w, 55);
-      if (ok) {
+      if (mbar_wait_warp(kv_full, 0, w, 55)) {
         e4m3_row_to_bf16(smem_u32(smem + C::K_OFF), t, 1.f);
         e4m3_row_to_bf16(smem_u32(smem + C::K_OFF), t + 64, 1.f);
         fence_proxy_async_smem();
         mbar_arrive(k_ready);
-      }
-      ItemCursor<GEN> cur;
-      cur.qb_first = qb_first;
-      cur.q_blocks = a.q_blocks;
-      cur.seek(a, kvs, item0);
-      for (int i = 0; ok && i < n_items && cur.next(a, kvs); ++i) {
-        const int st = i & 1;
-        if (!mbar_wait_warp(&qdo_full[st], (i >> 1) & 1, w, 56)) break;
-        const float* qsc = a.q_scale + static_cast<long long>(cur.qs) * a.S + cur.qb * BQ;
-        const uint32_t tile = smem_u32(smem + C::Q_OFF + st * C::TILE);
-        e4m3_row_to_bf16(tile, t, qsc[t]);
-        e4m3_row_to_bf16(tile, t + 64, qsc[t + 64]);
-        fence_proxy_async_smem();
-        mbar_arrive(&q_ready[st]);
       }
     } else if (warp >= 12) {
       // ---------------- dQ: one query row per thread ----------------

@@ -377,16 +377,18 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// Two E4M3 codes (the low byte first) to fp32, exactly (every E4M3 value is
-// an f16 value).
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
-  uint32_t h;
-  float lo, hi;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two_codes)));
-  asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, u;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h));
-  return make_float2(lo, hi);
+// Two E4M3 codes (bytes 0 and 1 of `two`) to fp32, exactly, on the integer
+// and FMA pipes: a code's 7 magnitude bits placed at fp32 bits 20..26 form an
+// fp32 number whose exponent field is the code's (with bias 127 instead of 7,
+// and a denormal where the code is subnormal), so one multiply by 2^120 --
+// exact, denormal inputs kept -- gives the code's value; the sign bit moves
+// to bit 31.
+__device__ __forceinline__ uint64_t e4m3x2_to_f2(uint32_t two) {
+  const uint32_t lo = ((two & 0x7Fu) << 20) | ((two & 0x80u) << 24);
+  const uint32_t hi = ((two & 0x7F00u) << 12) | ((two & 0x8000u) << 16);
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(((uint64_t)hi << 32) | lo), "l"(0x7B8000007B800000ull));
+  return r;
 }
 __device__ __forceinline__ float ex2(float x) {
   float y;
