@@ -42,6 +42,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "upipe_internal.h"
@@ -386,22 +387,31 @@ __global__ void __launch_bounds__(512, 1)
           // this half row of S^T in one load (one wait)
           uint32_t v[64];
           tmem_ld64(tmem + lane_off + C::T_S + half * 64, v);
+          // the causal mask only on the diagonal block, outside the unrolled
+          // loop, so the off-diagonal loop is straight-line code
+          auto p_loop = [&](auto masked) {
 #pragma unroll
-          for (int q0 = 0; q0 < 64; q0 += 4) {  // within this half
-            const int e = q0;
-            const float4 l4 = *reinterpret_cast<const float4*>(lse + q0);
-            const uint64_t xa = fma2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, f2(l4.x, l4.y));
-            const uint64_t xb = fma2(f2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), sl2x2, f2(l4.z, l4.w));
-            float p0 = ex2(f2_lo(xa)), p1 = ex2(f2_hi(xa)), p2 = ex2(f2_lo(xb)), p3 = ex2(f2_hi(xb));
-            if (diag) {
-              if (half * 64 + q0 < row) p0 = 0.f;
-              if (half * 64 + q0 + 1 < row) p1 = 0.f;
-              if (half * 64 + q0 + 2 < row) p2 = 0.f;
-              if (half * 64 + q0 + 3 < row) p3 = 0.f;
+            for (int q0 = 0; q0 < 64; q0 += 4) {  // within this half
+              const int e = q0;
+              const float4 l4 = *reinterpret_cast<const float4*>(lse + q0);
+              const uint64_t xa = fma2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, f2(l4.x, l4.y));
+              const uint64_t xb =
+                  fma2(f2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), sl2x2, f2(l4.z, l4.w));
+              float p0 = ex2(f2_lo(xa)), p1 = ex2(f2_hi(xa)), p2 = ex2(f2_lo(xb)), p3 = ex2(f2_hi(xb));
+              if (decltype(masked)::value) {
+                if (half * 64 + q0 < row) p0 = 0.f;
+                if (half * 64 + q0 + 1 < row) p1 = 0.f;
+                if (half * 64 + q0 + 2 < row) p2 = 0.f;
+                if (half * 64 + q0 + 3 < row) p3 = 0.f;
+              }
+              pk[q0 >> 1] = pack_bf16(p0, p1);
+              pk[(q0 >> 1) + 1] = pack_bf16(p2, p3);
             }
-            pk[q0 >> 1] = pack_bf16(p0, p1);
-            pk[(q0 >> 1) + 1] = pack_bf16(p2, p3);
-          }
+          };
+          if (diag)
+            p_loop(std::true_type{});
+          else
+            p_loop(std::false_type{});
         }
         // P^T (bf16 pairs) into the first 32 columns of this half's own S^T
         // columns, which only this thread has read
