@@ -60,7 +60,6 @@ struct BwdArgs {
   int q_split;  // CTAs per KV block, each a contiguous share of its items (dK, dV added atomically)
   float scale_log2, scale;
   int accumulate_kv;
-  int dq_tiled;
   int grp_slots;  // KV slots per group of the CTA order (divides n_kvslots)
   uint16_t kv_slot[kMaxSlots];
   const float* lse2;
@@ -132,8 +131,8 @@ __device__ __forceinline__ void e4m3_row_to_bf16(uint32_t tile, int r, float sca
   for (int u = 0; u < 8; ++u) {  // codes of columns 16u .. 16u + 15
     const uint32_t wds[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
     uint32_t o[8];
-#pragma unroll
     const uint64_t sc = f2(scale, scale);
+#pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint64_t a = mul2(e4m3x2_to_f2(wds[k] & 0xFFFFu), sc), b = mul2(e4m3x2_to_f2(wds[k] >> 16), sc);
       o[2 * k] = pack_bf16(f2_lo(a), f2_hi(a));
@@ -162,7 +161,7 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* s_full = bars + 5;
   uint64_t* dp_full = bars + 6;
   uint64_t* p_ready = bars + 7;
-  uint64_t* dq_staged = bars + 8;  // [2] per Q/dO stage: its item's dQ has been read out of it (TMA mode)
+  uint64_t* dq_staged = bars + 8;  // [2] per Q/dO stage: its item's dQ has been read out of it
   uint64_t* ds_ready = bars + 10;
   uint64_t* ds_consumed = bars + 11;
   uint64_t* dq_full = bars + 12;
@@ -254,8 +253,8 @@ __global__ void __launch_bounds__(512, 1)
       for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
         const int st = i & 1;
         if (!mbar_wait(&qdo_empty[st], ((i >> 1) & 1) ^ 1, w, 40)) break;
-        // in the TMA reduce mode the stage's previous item staged its dQ here
-        if (a.dq_tiled == 2 && !mbar_wait(&dq_staged[st], ((i >> 1) & 1) ^ 1, w, 39)) break;
+        // the stage's previous item staged its dQ here
+        if (!mbar_wait(&dq_staged[st], ((i >> 1) & 1) ^ 1, w, 39)) break;
         const long long q_row = static_cast<long long>(cur.qs) * a.S + cur.qb * BQ;
         mbar_arrive_expect_tx(&qdo_full[st], (F8 ? CH : C::TILE) + C::TILE + 2 * BQ * 4);
 #pragma unroll
@@ -501,8 +500,8 @@ __global__ void __launch_bounds__(512, 1)
     } else if (warp >= 12) {
       // ---------------- dQ: one query row per thread ----------------
       // dQ_i leaves TMEM (freeing dP's columns for dP_{i+1}) and is added into
-      // the global fp32 accumulator with vector reductions, off the softmax
-      // warps' path
+      // the global fp32 accumulator by the TMA engine, off the softmax warps'
+      // path
       const int row = (warp & 3) * 32 + lane;
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
       // dQ = dS K / sqrt(d); FP8: K's block scale as well (K's tile holds its codes)
@@ -511,91 +510,63 @@ __global__ void __launch_bounds__(512, 1)
       cur.qb_first = qb_first;
       cur.q_blocks = a.q_blocks;
       cur.seek(a, kvs, item0);
-      if (a.dq_tiled == 2) {
-        // row-major fp32 dQ through the TMA engine: each warp stages its 32
-        // rows in 32-column chunks (32 x 32 fp32, 128-byte swizzle, 4 KB)
-        // in its quarter of step i's Q/dO buffer -- the first D/64 chunks in
-        // the dO tile (free: dV_i, its last reader, ran before dQ_i), the
-        // rest in the Q tile once dK_i has completed -- and issues element-
-        // wise reduce-adds; when the engine has read them, the buffer goes
-        // back to the producer
-        tma_prefetch_map(&tmDQ);
-        constexpr int NCH = D / 32, HALF = NCH / 2;
-        const uint32_t quarter = (warp & 3) * (C::TILE / 4);
-        for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
-          const int st = i & 1;
-          if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
-          tc_fence_after();
-          const int y0 = cur.qs * a.S + cur.qb * BQ + (warp & 3) * 32;
-          const uint32_t s_stage = smem_u32(smem) + st * C::TILE + quarter;
-          bool ok = true;
+      // row-major fp32 dQ through the TMA engine: each warp stages its 32
+      // rows in 32-column chunks (32 x 32 fp32, 128-byte swizzle, 4 KB)
+      // in its quarter of step i's Q/dO buffer -- the first D/64 chunks in
+      // the dO tile (free: dV_i, its last reader, ran before dQ_i), the
+      // rest in the Q tile once dK_i has completed -- and issues element-
+      // wise reduce-adds; when the engine has read them, the buffer goes
+      // back to the producer
+      tma_prefetch_map(&tmDQ);
+      constexpr int NCH = D / 32, HALF = NCH / 2;
+      const uint32_t quarter = (warp & 3) * (C::TILE / 4);
+      for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
+        const int st = i & 1;
+        if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
+        tc_fence_after();
+        const int y0 = cur.qs * a.S + cur.qb * BQ + (warp & 3) * 32;
+        const uint32_t s_stage = smem_u32(smem) + st * C::TILE + quarter;
+        bool ok = true;
 #pragma unroll 1
-          for (int c = 0; ok && c < D / 64; ++c) {
-            uint32_t v[64];
-            tmem_ld64(tmem + lane_off + C::T_DP + c * 64, v);
-            if (c == D / 64 - 1) {
-              tc_fence_before();
-              mbar_arrive(dq_drained);
+        for (int c = 0; ok && c < D / 64; ++c) {
+          uint32_t v[64];
+          tmem_ld64(tmem + lane_off + C::T_DP + c * 64, v);
+          if (c == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(dq_drained);
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int chunk = 2 * c + h;
+            if (chunk == HALF && !mbar_wait_warp(&qdo_empty[st], (i >> 1) & 1, w, 54)) {
+              ok = false;
+              break;
             }
+            const uint32_t buf = s_stage + (chunk < HALF ? C::DO_OFF : C::Q_OFF) + (chunk % HALF) * 4096;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int chunk = 2 * c + h;
-              if (chunk == HALF && !mbar_wait_warp(&qdo_empty[st], (i >> 1) & 1, w, 54)) {
-                ok = false;
-                break;
-              }
-              const uint32_t buf = s_stage + (chunk < HALF ? C::DO_OFF : C::Q_OFF) + (chunk % HALF) * 4096;
-#pragma unroll
-              for (int p = 0; p < 8; ++p)
-                st_shared_v4(buf + lane * 128 + ((p ^ (lane & 7)) << 4),
-                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p]) * dq_mul),
-                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 1]) * dq_mul),
-                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 2]) * dq_mul),
-                             __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 3]) * dq_mul));
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                tma_reduce_add_2d(&tmDQ, buf, chunk * 32, y0);
-                bulk_commit();
-              }
+            for (int p = 0; p < 8; ++p)
+              st_shared_v4(buf + lane * 128 + ((p ^ (lane & 7)) << 4),
+                           __float_as_uint(__uint_as_float(v[h * 32 + 4 * p]) * dq_mul),
+                           __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 1]) * dq_mul),
+                           __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 2]) * dq_mul),
+                           __float_as_uint(__uint_as_float(v[h * 32 + 4 * p + 3]) * dq_mul));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_2d(&tmDQ, buf, chunk * 32, y0);
+              bulk_commit();
             }
           }
-          if (!ok) break;
-          if (lane == 0) {
-            bulk_wait_read<0>();
-            mbar_arrive(&dq_staged[st]);
-          }
-          __syncwarp();
         }
-        if (lane == 0) bulk_wait_all();
+        if (!ok) break;
+        if (lane == 0) {
+          bulk_wait_read<0>();
+          mbar_arrive(&dq_staged[st]);
+        }
         __syncwarp();
-      } else {
-        // vector reductions from the registers, tiled or row-major
-        for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
-          if (!mbar_wait_warp(dq_full, i & 1, w, 53)) break;
-          tc_fence_after();
-          const long long qrow = static_cast<long long>(cur.qs) * a.S + cur.qb * BQ + row;
-          // address of the 4 columns starting at column 4*g of query row qrow
-          auto col4 = [&](int g) -> float* {
-            return a.dq_tiled ? a.dQacc + ((qrow >> 5) * (D / 4) + g) * 128 + (qrow & 31) * 4
-                              : a.dQacc + qrow * D + 4 * g;
-          };
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            uint32_t v[64];
-            tmem_ld64(tmem + lane_off + C::T_DP + c * 64, v);
-            if (c == D / 64 - 1) {
-              tc_fence_before();
-              mbar_arrive(dq_drained);
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              red_add_v4(col4(c * 16 + e), __uint_as_float(v[4 * e]) * dq_mul,
-                         __uint_as_float(v[4 * e + 1]) * dq_mul, __uint_as_float(v[4 * e + 2]) * dq_mul,
-                         __uint_as_float(v[4 * e + 3]) * dq_mul);
-          }
-        }
       }
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   } else if (aligned && n_items == 0 && !a.accumulate_kv && q_split == 1 && warp >= 4 && warp < 12) {
     // a KV slot no query head uses in this launch: its gradient is zero
@@ -648,32 +619,6 @@ __global__ void bwd_prep_kernel(const BwdPrepDesc p) {
   }
 }
 
-// Tiled fp32 dQ -> bf16 rows of the sequence layout, through shared memory:
-// one block per (32-token group, slot); reads are 512-byte runs, writes are
-// whole d-wide row segments.
-__global__ void __launch_bounds__(256) dq_tiled_to_seq_kernel(const DqTiledDesc p) {
-  __shared__ float tile[32][128 + 1];
-  const int groups = p.S / 32;
-  const int g = static_cast<int>(blockIdx.x) % groups;
-  const int k = static_cast<int>(blockIdx.x) / groups;
-  const int quads = p.D / 4;
-  const float* src = p.src + (static_cast<long long>(k) * groups + g) * quads * 128;
-  for (int idx = threadIdx.x; idx < 32 * quads; idx += blockDim.x) {
-    const int q = idx / 32, r = idx % 32;
-    const float4 x = *reinterpret_cast<const float4*>(src + q * 128 + r * 4);
-    tile[r][4 * q] = x.x; tile[r][4 * q + 1] = x.y; tile[r][4 * q + 2] = x.z; tile[r][4 * q + 3] = x.w;
-  }
-  __syncthreads();
-  const int vpr = p.D / 8;
-  for (int idx = threadIdx.x; idx < 32 * vpr; idx += blockDim.x) {
-    const int r = idx / vpr, v = idx % vpr;
-    const float* f = &tile[r][8 * v];
-    uint16_t* out = p.dst + (static_cast<long long>(g) * 32 + r) * p.ld_dst + static_cast<long long>(p.dst_head[k]) * p.D + 8 * v;
-    *reinterpret_cast<uint4*>(out) = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                                                pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
-  }
-}
-
 template <int D, bool GEN, bool F8 = false>
 cudaError_t run_bwd(const CUtensorMap* tm, const BwdArgs& args, cudaStream_t st) {
   auto kern = attn_bwd_kernel<D, GEN, F8>;
@@ -698,12 +643,6 @@ cudaError_t launch_bwd_prep(const BwdPrepDesc& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_dq_tiled_to_seq(const DqTiledDesc& p, cudaStream_t st) {
-  if ((p.D != 64 && p.D != 128) || p.S % 32 || p.n_slots <= 0 || p.n_slots > kMaxSlots) return cudaErrorInvalidValue;
-  dq_tiled_to_seq_kernel<<<(p.S / 32) * p.n_slots, 256, 0, st>>>(p);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) {
   const int kv_len = d.kv_len ? d.kv_len : d.S;
   const int kv_ld = d.kv_ld ? d.kv_ld : kv_len;
@@ -714,9 +653,8 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) 
   if (d.q_split < 1 || d.q_split > 16) return cudaErrorInvalidValue;
   for (int i = 0; i < d.n_qslots; ++i)
     if (d.kv_slot[i] >= d.n_kvslots) return cudaErrorInvalidValue;
-  if (d.dq_tiled < 0 || d.dq_tiled > 2) return cudaErrorInvalidValue;
   CUtensorMap tm[5];
-  if (d.fp8 && (d.D != 128 || !d.q_scale || !d.k_scale || d.dq_tiled != 2)) return cudaErrorInvalidValue;
+  if (d.fp8 && (d.D != 128 || !d.q_scale || !d.k_scale)) return cudaErrorInvalidValue;
   if (d.fp8) {  // Q and K codes: one 128 x 128 byte box per tile
     if (!make_tmap_u8(&tm[0], d.Q, d.D, (uint64_t)d.n_qslots * d.S, d.D, 128, 128)) return cudaErrorInvalidValue;
     if (!make_tmap_u8(&tm[1], d.K, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 128, 128)) return cudaErrorInvalidValue;
@@ -726,12 +664,8 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) 
   }
   if (!make_tmap_bf16(&tm[2], d.V, d.D, (uint64_t)d.n_kvslots * kv_ld, d.D, 64, 128)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tm[3], d.dO, d.D, (uint64_t)d.n_qslots * d.S, d.D, 64, 128)) return cudaErrorInvalidValue;
-  // dQ accumulator as fp32 rows for the TMA reduce mode (otherwise unused)
-  if (d.dq_tiled == 2) {
-    if (!make_tmap_f32(&tm[4], d.dQacc, d.D, (uint64_t)d.n_qslots * d.S, d.D, 32, 32)) return cudaErrorInvalidValue;
-  } else {
-    tm[4] = tm[3];
-  }
+  // the dQ accumulator as fp32 rows, for the TMA reduce-adds
+  if (!make_tmap_f32(&tm[4], d.dQacc, d.D, (uint64_t)d.n_qslots * d.S, d.D, 32, 32)) return cudaErrorInvalidValue;
   BwdArgs a;
   a.S = d.S;
   a.kv_ld = kv_ld;
@@ -744,7 +678,6 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& d, int* status, cudaStream_t st) 
   a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.D)));
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d.D)));
   a.accumulate_kv = d.accumulate_kv;
-  a.dq_tiled = d.dq_tiled;
   // at most 2^20 tokens of query-side data per group of concurrently running
   // slots (8 slots up to S = 128K, fewer beyond), a divisor of n_kvslots
   int g = std::max(1, std::min(8, (1 << 20) / d.S));

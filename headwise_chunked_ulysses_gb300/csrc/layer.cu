@@ -628,7 +628,6 @@ int attention_bwd_enqueue(const void* Q, const void* K, const void* V, const voi
   AttnBwdDesc ab;
   ab.Q = Q; ab.K = K; ab.V = V; ab.dO = dO; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dQ; ab.dK = dK; ab.dV = dV;
   ab.accumulate_kv = 0; ab.S = S; ab.D = d_head; ab.n_qslots = n_q; ab.n_kvslots = n_kv;
-  ab.dq_tiled = 2;  // row-major dQ added by TMA reduce-adds, as in the layer
   for (int k = 0; k < n_q; ++k) ab.kv_slot[k] = static_cast<uint16_t>(kv_of_q[k]);
   return launch_attn_bwd(ab, status, st) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;
 }
@@ -892,7 +891,6 @@ int attn_bwd_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const upipe_bf1
     ab.dK = dacc + U * slot_elems;
     ab.dV = dacc + (U + p.n_kv_slots) * slot_elems;
     ab.accumulate_kv = (ooo && i > 0) ? 1 : 0;
-    ab.dq_tiled = 2;
     ab.S = S; ab.D = d; ab.n_qslots = U; ab.n_kvslots = p.n_kv_slots;
     for (int k = 0; k < U; ++k) ab.kv_slot[k] = static_cast<uint16_t>(g.kv_of_q[k]);
     L.bwd(ab);
@@ -1284,7 +1282,6 @@ int upipe_attention_bwd_fp8(const uint8_t* Q, const float* q_scale, const uint8_
   AttnBwdDesc ab;
   ab.Q = Q; ab.K = K; ab.V = V; ab.dO = dO; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dQ; ab.dK = dK; ab.dV = dV;
   ab.accumulate_kv = 0; ab.S = S; ab.D = d_head; ab.n_qslots = n_q; ab.n_kvslots = n_kv;
-  ab.dq_tiled = 2;
   ab.fp8 = true; ab.q_scale = q_scale; ab.k_scale = k_scale;
   for (int k = 0; k < n_q; ++k) ab.kv_slot[k] = static_cast<uint16_t>(kv_of_q[k]);
   return launch_attn_bwd(ab, status, st) == cudaSuccess ? UPIPE_OK : UPIPE_ECUDA;

@@ -444,7 +444,7 @@ int attn_bwd_chunked_issue(const upipe_bf16* X, const upipe_bf16* W_qkv, const u
       const int n_out = U + (final_here ? 2 * nkv : 0);
       const long long ld_dseq = static_cast<long long>(n_out) * d;
       AttnBwdDesc ab;
-      ab.Q = qh; ab.dO = doh; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dq; ab.dq_tiled = 2;
+      ab.Q = qh; ab.dO = doh; ab.lse2 = lse2; ab.Dsum = dsum; ab.dQacc = dq;
       ab.S = Sc; ab.D = d; ab.n_qslots = U; ab.n_kvslots = nkv;
       ab.kv_len = Sc; ab.kv_ld = Sc;
       ab.accumulate_kv = acc ? 1 : 0;

@@ -78,12 +78,9 @@ struct AttnBwdDesc {
   const void* dO = nullptr;  // [n_qslots][S][D] bf16
   const float* lse2 = nullptr;  // [n_qslots][S]  minus the log-sum-exp in log2 units
   const float* Dsum = nullptr;  // [n_qslots][S]  rowsum(dO * O)
-  float* dQacc = nullptr;    // fp32 per query slot, pre-zeroed, atomically accumulated
-  // dQacc layout: 0 = [slot][S][D] row-major; 1 = tiled [slot][S/32][D/4][32][4]
-  // (32 consecutive rows of one 4-wide column group contiguous, so one warp's
-  // vector reduction covers a single 512-byte run); 2 = row-major, added by
-  // TMA reduce-adds of 32 x 32 chunks staged in shared memory
-  int dq_tiled = 0;
+  // fp32 per query slot, [slot][S][D] row-major, pre-zeroed; every KV block
+  // adds its share by TMA reduce-adds of 32 x 32 chunks staged in shared memory
+  float* dQacc = nullptr;
   float* dK = nullptr;       // [n_kvslots][kv_ld][D] fp32
   float* dV = nullptr;       // [n_kvslots][kv_ld][D] fp32
   int accumulate_kv = 0;     // add into dK/dV instead of overwriting
@@ -95,7 +92,7 @@ struct AttnBwdDesc {
   // into buffers that hold zeros or earlier partial sums (accumulate_kv is
   // then implied and nothing is zero-filled)
   int q_split = 1;
-  // FP8 heads (plain launch, D = 128, dq_tiled = 2): Q and K hold E4M3 codes,
+  // FP8 heads (plain launch, D = 128): Q and K hold E4M3 codes,
   // one byte each, with q_scale [n_qslots][S] and k_scale [n_kvslots][kv_ld / 128]
   bool fp8 = false;
   const float* q_scale = nullptr;
@@ -118,13 +115,6 @@ struct Head2SeqDesc {
   uint16_t dst_head[kMaxSlots];     // output head -> head block in a dest row
   uint16_t first[kMaxSlots + 1];    // CSR over source slots per output head
   uint16_t src_slot[kMaxSlots];     // summed in this order (fp32)
-};
-// Tiled fp32 dQ (see AttnBwdDesc::dq_tiled) -> bf16 sequence layout.
-struct DqTiledDesc {
-  const float* src = nullptr;                   // [n_slots][S/32][D/4][32][4]
-  uint16_t* dst = nullptr; long long ld_dst = 0; // bf16 [S][row]
-  int S = 0, D = 0, n_slots = 0;
-  uint16_t dst_head[kMaxSlots];                 // slot -> head block in a dest row
 };
 struct BwdPrepDesc {
   const uint16_t* dO = nullptr; long long ld_do = 0;  // seq layout
@@ -161,7 +151,6 @@ cudaError_t launch_attn_bwd(const AttnBwdDesc& a, int* status, cudaStream_t st);
 cudaError_t launch_seq2head(const Seq2HeadDesc& p, cudaStream_t st);
 cudaError_t launch_head2seq(const Head2SeqDesc& p, cudaStream_t st);
 cudaError_t launch_bwd_prep(const BwdPrepDesc& p, cudaStream_t st);
-cudaError_t launch_dq_tiled_to_seq(const DqTiledDesc& p, cudaStream_t st);
 cudaError_t launch_quant_e4m3(const QuantDesc& p, cudaStream_t st);
 
 // Tensor maps (driver entry point resolved through the runtime).
