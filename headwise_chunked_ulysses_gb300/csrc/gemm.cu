@@ -217,7 +217,9 @@ __global__ void __launch_bounds__(256, 1)
           tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 32, v);
           const int n = n0 + c * 32;
           const int oc = g.use_omap_n ? g.omap_n[n >> 6] * 64 + (n & 63) : n;
-          store_tile_chunk(g, m, oc, v);
+          // the last row tile of an M that is a multiple of 64 only: its A
+          // rows past M were read as zeros and its rows past M are not written
+          if (m < g.M) store_tile_chunk(g, m, oc, v);
         }
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
@@ -526,7 +528,7 @@ void copy_map(const BlockMap& m, int& use, uint16_t* dst) {
 }  // namespace
 
 cudaError_t launch_gemm(const GemmDesc& d, int* status, cudaStream_t st) {
-  if (d.M % BM || d.K % BK || d.N % 64 || d.M <= 0 || d.N <= 0 || d.K <= 0) return cudaErrorInvalidValue;
+  if (d.M % 64 || d.K % BK || d.N % 64 || d.M <= 0 || d.N <= 0 || d.K <= 0) return cudaErrorInvalidValue;
   if (d.split_k < 1 || (d.K / BK) % d.split_k || (d.split_k > 1 && d.out_mode != kOutF32Red))
     return cudaErrorInvalidValue;
   const int BN = (d.N % 256 == 0) ? 256 : (d.N % 128 == 0 ? 128 : 64);
@@ -535,7 +537,7 @@ cudaError_t launch_gemm(const GemmDesc& d, int* status, cudaStream_t st) {
   if (!make_tmap_bf16(&tb, d.B, d.b_cols, d.b_rows, d.ldb, 64, 64)) return cudaErrorInvalidValue;
   GemmArgs a;
   a.M = d.M; a.N = d.N; a.K = d.K;
-  a.m_tiles = d.M / BM;
+  a.m_tiles = (d.M + BM - 1) / BM;  // a last tile of 64 rows reads zeros past M
   a.n_tiles = d.N / BN;
   a.split_k = d.split_k;
   copy_map(d.amap_k, a.use_amap_k, a.amap_k);

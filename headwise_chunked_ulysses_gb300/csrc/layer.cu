@@ -157,7 +157,7 @@ int check_shape(const Shape& s) {
   if (s.sched != UPIPE_SCHED_INORDER && s.sched != UPIPE_SCHED_GQA_OOO) return UPIPE_EINVAL;
   if (s.H % s.U || s.U % s.C || s.H % s.G || s.S % s.C) return UPIPE_EINVAL;
   if (s.sched == UPIPE_SCHED_GQA_OOO && !(s.G % s.C == 0 || s.C % s.G == 0)) return UPIPE_EINVAL;
-  if (s.S % 128 || s.dm % 128) return UPIPE_EINVAL;
+  if (s.S % 128 || s.dm % 64) return UPIPE_EINVAL;
   if (s.d != 64 && s.d != 128) return UPIPE_EUNSUPPORTED;
   // widest stage buffer, in heads: the stage's queries plus the K and V heads it moves
   const int kv_moved = s.sched == UPIPE_SCHED_GQA_OOO ? std::max(s.G, s.C) : std::min(s.U, s.G);
@@ -346,7 +346,7 @@ bool all_stages_fp8(const Plan& p, const uint8_t* fp8_heads) {
 // smallest split giving at least 4 tiles per SM, K/64 divisible by it.
 int choose_split_k(const GemmDesc& g) {
   const int bn = (g.N % 256 == 0) ? 256 : (g.N % 128 == 0 ? 128 : 64);
-  const long long tiles = static_cast<long long>(g.M / 128) * (g.N / bn);
+  const long long tiles = static_cast<long long>((g.M + 127) / 128) * (g.N / bn);
   const int kb = g.K / 64;
   int best = 1;
   for (int s = 1; s <= 16; ++s) {
@@ -1302,7 +1302,7 @@ int upipe_attention_bwd(const upipe_bf16* Q, const upipe_bf16* K, const upipe_bf
 int upipe_gemm_bf16(const upipe_bf16* A, const upipe_bf16* B, void* D, int M, int N, int K, int a_trans, int b_trans,
                     long long lda, long long ldb, long long ldd, int out_mode, void* stream) {
   if (!A || !B || !D || !aligned16(A) || !aligned16(B) || !aligned16(D)) return UPIPE_EINVAL;
-  if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 64 || K % 64) return UPIPE_EINVAL;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 64 || N % 64 || K % 64) return UPIPE_EINVAL;
   if (out_mode < 0 || out_mode > 3 || lda % 8 || ldb % 8 || ldd % 8) return UPIPE_EINVAL;
   if (!device_supported()) return UPIPE_EUNSUPPORTED;
   int* status = status_ptr();

@@ -46,7 +46,7 @@
  *     UPIPE_ECUDA (a launch failed) and UPIPE_ETIMEOUT.
  *   - Shape rules (method constraints and kernel tiling): U | H (stages of U
  *     heads), C | U (U/C heads per rank; the pages' Limitations section),
- *     G | H, C | S, S % 128 == 0, d_model % 128 == 0, d_head in {64, 128},
+ *     G | H, C | S, S % 128 == 0, d_model % 64 == 0, d_head in {64, 128},
  *     H + 2G <= 256 heads in one stage; the out-of-order schedule also needs
  *     C | G or G | C.
  */
@@ -404,7 +404,7 @@ int upipe_attention_bwd_noalloc(const upipe_bf16* Q, const upipe_bf16* K, const 
  *   out_mode 0: D bf16;  1: D fp32;  2: D fp32 += A B;  3: D fp32 += A B with K
  *   split across CTAs and the partial sums added by fp32 atomics (for few output
  *   tiles and a long K; the summation order varies between runs).  ldd: row stride of D.
- * M % 128 == 0, N % 64 == 0, K % 64 == 0.
+ * M % 64 == 0, N % 64 == 0, K % 64 == 0.
  */
 int upipe_gemm_bf16(const upipe_bf16* A, const upipe_bf16* B, void* D, int M, int N, int K, int a_trans, int b_trans,
                     long long lda, long long ldb, long long ldd, int out_mode, void* stream);

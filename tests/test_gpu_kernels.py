@@ -64,7 +64,9 @@ def test_exchange_is_bit_exact(up, S, n_heads, d, C, pad):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("M,N,K", [(256, 384, 320), (128, 512, 128), (384, 64, 192), (256, 256, 1024),
-                                   (128, 256, 8192), (512, 512, 512), (768, 1280, 576), (256, 256, 16384)])
+                                   (128, 256, 8192), (512, 512, 512), (768, 1280, 576), (256, 256, 16384),
+                                   # M a multiple of 64 only: a last row tile of 64 rows
+                                   (64, 256, 192), (192, 384, 320), (320, 1536, 8192)])
 @pytest.mark.parametrize("a_trans,b_trans", [(0, 0), (0, 1), (1, 0), (1, 1)])
 def test_gemm_layouts_and_modes(up, M, N, K, a_trans, b_trans):
     import torch

@@ -139,6 +139,21 @@ def test_u_invariance_across_stages(up, tiny):
             assert rel(outs[U][k], outs[8][k]) <= TOL, (U, k)
 
 
+@pytest.mark.parametrize("shape,U,C,sched", [
+    (LayerShape(S=512, d_model=192, H=4, G=2, d_head=64, U=2, C=2), 2, 2, 0),
+    (LayerShape(S=512, d_model=192, H=4, G=2, d_head=64, U=2, C=2), 2, 2, 1),
+    (LayerShape(S=384, d_model=320, H=4, G=1, d_head=128, U=4, C=2), 4, 2, 0),
+    (LayerShape(S=256, d_model=64, H=2, G=2, d_head=64, U=1, C=1), 1, 1, 0)])
+def test_d_model_a_multiple_of_64(up, shape, U, C, sched):
+    """Model widths that are multiples of 64 but not of 128: the contractions
+    with d_model as their row count (dW_qkv = X^T dQKV) end in a 64-row tile."""
+    ref = Ref(shape, seed=5)
+    out = _run(up, ref, U, C, sched, check_guards=True)
+    e = _errors(ref, out)
+    assert max(e["Y"], e["O"], e["dX"], e["dW_qkv"], e["dW_o"]) <= TOL, e
+    assert e["lse_abs"] < LSE_TOL, e
+
+
 @pytest.mark.parametrize("sched", [0, 1])
 def test_llama_widths_4k(up, sched):
     ref = Ref(SHAPES["llama3_8b_4k"])
