@@ -342,17 +342,30 @@ bool all_stages_fp8(const Plan& p, const uint8_t* fp8_heads) {
   return true;
 }
 
-// Split of a long-K contraction so that its output tiles fill the GPU: the
-// smallest split giving at least 4 tiles per SM, K/64 divisible by it.
+// Split of a long-K contraction over CTAs (partial sums added atomically):
+// of the splits s <= 8 that divide its K blocks into runs of at least 8 and
+// whose s fp32 partial outputs come to at most 256 MB of reduce-adds, the
+// one whose s x (output tiles) work units fill the last round of the GPU's
+// tile slots best (CTA pairs for 256 x 256 tiles, one CTA otherwise); a
+// larger split must fill it at least 2 % better.
 int choose_split_k(const GemmDesc& g) {
   const int bn = (g.N % 256 == 0) ? 256 : (g.N % 128 == 0 ? 128 : 64);
-  const long long tiles = static_cast<long long>((g.M + 127) / 128) * (g.N / bn);
+  const bool pair = bn == 256 && g.M % 256 == 0 && num_sms() >= 2;
+  const long long tiles = pair ? static_cast<long long>(g.M / 256) * (g.N / 256)
+                               : static_cast<long long>((g.M + 127) / 128) * (g.N / bn);
+  const long long slots = pair ? num_sms() / 2 : num_sms();
   const int kb = g.K / 64;
   int best = 1;
-  for (int s = 1; s <= 16; ++s) {
+  double best_fill = -1.0;
+  for (int s = 1; s <= 8; ++s) {
     if (kb % s || kb / s < 8) continue;
-    best = s;
-    if (tiles * s >= 4LL * num_sms()) break;
+    if (s > 1 && static_cast<long long>(s) * g.M * g.N * 4 > (1LL << 28)) break;
+    const long long units = tiles * s, rounds = (units + slots - 1) / slots;
+    const double fill = static_cast<double>(units) / static_cast<double>(rounds * slots);
+    if (fill > best_fill + 0.02) {
+      best = s;
+      best_fill = fill;
+    }
   }
   return best;
 }
