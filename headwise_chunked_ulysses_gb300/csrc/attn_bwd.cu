@@ -426,15 +426,13 @@ __global__ void __launch_bounds__(512, 1)
           tmem_ld32(tmem + lane_off + C::T_DP + half * 64 + c * 32, v);
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
+            // dP^T - D in fp32, rounded to bf16, times the bf16 P^T it pairs with
             const int q0 = c * 32 + e;
             const float4 d4 = *reinterpret_cast<const float4*>(Dv + q0);
-            const uint32_t pa = pk[q0 >> 1], pb = pk[(q0 >> 1) + 1];
-            const uint64_t da = mul2(f2(bf16_lo(pa), bf16_hi(pa)),
-                                     sub2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), f2(d4.x, d4.y)));
-            const uint64_t db = mul2(f2(bf16_lo(pb), bf16_hi(pb)),
-                                     sub2(f2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), f2(d4.z, d4.w)));
-            pk[q0 >> 1] = pack_bf16(f2_lo(da), f2_hi(da));
-            pk[(q0 >> 1) + 1] = pack_bf16(f2_lo(db), f2_hi(db));
+            const uint64_t ta = sub2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), f2(d4.x, d4.y));
+            const uint64_t tb = sub2(f2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), f2(d4.z, d4.w));
+            pk[q0 >> 1] = mul_bf16x2(pk[q0 >> 1], pack_bf16(f2_lo(ta), f2_hi(ta)));
+            pk[(q0 >> 1) + 1] = mul_bf16x2(pk[(q0 >> 1) + 1], pack_bf16(f2_lo(tb), f2_hi(tb)));
           }
         }
         // the dS^T tile is free once the previous step's dQ MMA has read it

@@ -401,7 +401,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-// Per-warpgroup register budget (all 128 threads of the warpgroup execute it).
+// Packed pairs of bf16: a * b, rounded to nearest even.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 // Packed pairs of fp32 (one 64-bit register) for the f32x2 arithmetic of sm_100+.
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
   uint64_t r;
