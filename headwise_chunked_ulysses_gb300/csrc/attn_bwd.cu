@@ -19,14 +19,16 @@
 // MMAs and the softmax are the bf16 ones.  The gradients in Q and K are those of the dequantized
 // operands (the rounding to E4M3 passed through as the identity).
 //
-// One CTA per (KV slot, 128-row KV block).  It walks every query slot mapped
-// to its KV slot and every query block at or after its KV block, so the GQA
+// One CTA per (KV slot, 128-row KV block), ordered in groups of two KV slots
+// (block 0, the longest, first), so the CTAs running at one time keep two
+// slots' query-side data in L2.  A CTA walks every query slot mapped to its
+// KV slot and every query block at or after its KV block, so the GQA
 // reduction of dK/dV happens in TMEM with no atomics.  Per step i:
 //   S^T = K Q^T, dP^T = V dO^T  (tensor cores -> TMEM)
 //   warps 4..11, two per TMEM lane quarter, each thread owning half of one
 //     KV row (64 query columns): P^T as bf16 back into S^T's TMEM columns,
-//     then dS^T = P^T * (dP^T - D) as bf16 into the other half of those
-//     columns and into shared memory
+//     then dS^T = P^T * (dP^T - D) (dP^T - D in fp32, the product in packed
+//     bf16) into the other half of those columns and into shared memory
 //   dV += P^T dO and dK += dS^T Q (A operands read from TMEM), dQ = dS K
 //     (both operands in shared memory; dQ reuses dP's TMEM columns)
 //   warps 12..15, one query row per thread, move dQ_i out of TMEM and send
