@@ -571,38 +571,55 @@ def main():
                  "dW_o": torch.empty_like(dWo)}]
         hout = [outs, {k: torch.empty_like(v).pin_memory() for k, v in outs.items()}]
 
+        fwd_in, bwd_in = ("X", "W_qkv", "W_o"), ("dY",)
+
         def run_e2e(n):
+            # a step's forward needs X and the weights, its backward dY as
+            # well; Y leaves after the forward, the gradients after the
+            # backward, so the first step's dY copy and the last step's Y copy
+            # overlap compute too
             ev = lambda: torch.cuda.Event()
-            in_ready, in_free, out_ready, out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()], [ev(), ev()]
+            fwd_ready, bwd_ready, in_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+            y_ready, out_ready, out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+            def copy_in(b):
+                with torch.cuda.stream(h2d_s):
+                    for k in fwd_in:
+                        din[b][k].copy_(pin[k], non_blocking=True)
+                fwd_ready[b].record(h2d_s)
+                with torch.cuda.stream(h2d_s):
+                    for k in bwd_in:
+                        din[b][k].copy_(pin[k], non_blocking=True)
+                bwd_ready[b].record(h2d_s)
+
             start = ev()
             start.record(stream)
             h2d_s.wait_event(start)
-            with torch.cuda.stream(h2d_s):
-                for k in din[0]:
-                    din[0][k].copy_(pin[k], non_blocking=True)
-            in_ready[0].record(h2d_s)
+            copy_in(0)
             for i in range(n):
                 b = i & 1
                 if i + 1 < n:  # inputs of step i+1, once step i-1 has finished with that buffer
                     nb = b ^ 1
                     if i >= 1:
                         h2d_s.wait_event(in_free[nb])
-                    with torch.cuda.stream(h2d_s):
-                        for k in din[nb]:
-                            din[nb][k].copy_(pin[k], non_blocking=True)
-                    in_ready[nb].record(h2d_s)
-                stream.wait_event(in_ready[b])
+                    copy_in(nb)
+                stream.wait_event(fwd_ready[b])
                 if i >= 2:
                     stream.wait_event(out_free[b])
                 o = dout[b]
                 upipe.attn_fwd(din[b]["X"], din[b]["W_qkv"], din[b]["W_o"], s, Y=o["Y"], O_saved=O, lse=lse, ws=wsf)
+                y_ready[b].record(stream)
+                d2h_s.wait_event(y_ready[b])
+                with torch.cuda.stream(d2h_s):
+                    hout[b]["Y"].copy_(o["Y"], non_blocking=True)
+                stream.wait_event(bwd_ready[b])
                 upipe.attn_bwd(din[b]["X"], din[b]["W_qkv"], din[b]["W_o"], O, lse, din[b]["dY"], s, dX=o["dX"],
                                dW_qkv=o["dW_qkv"], dW_o=o["dW_o"], ws=wsb)
                 in_free[b].record(stream)
                 out_ready[b].record(stream)
                 d2h_s.wait_event(out_ready[b])
                 with torch.cuda.stream(d2h_s):
-                    for k in hout[b]:
+                    for k in ("dX", "dW_qkv", "dW_o"):
                         hout[b][k].copy_(o[k], non_blocking=True)
                 out_free[b].record(d2h_s)
             stream.wait_stream(d2h_s)
@@ -619,7 +636,8 @@ def main():
         e2e = {"value": aggregate_tokens_per_s(world, sh.S, args.steps, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps,
                "copies": "per step: all inputs host->device and Y, dX, dW_qkv, dW_o device->host, on two copy "
-                         "streams overlapping the neighbouring steps' compute (double-buffered on the device)"}
+                         "streams overlapping compute (double-buffered on the device; dY may arrive during the "
+                         "step's forward, Y leaves during its backward)"}
         upipe.sync_status()
 
     mem_peak = torch.cuda.max_memory_allocated(dev) - mem_before
