@@ -502,7 +502,6 @@ __global__ void __launch_bounds__(512, 1)
       // dQ_i leaves TMEM (freeing dP's columns for dP_{i+1}) and is added into
       // the global fp32 accumulator by the TMA engine, off the softmax warps'
       // path
-      const int row = (warp & 3) * 32 + lane;
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
       // dQ = dS K / sqrt(d); FP8: K's block scale as well (K's tile holds its codes)
       const float dq_mul = F8 ? a.scale * a.k_scale[static_cast<long long>(kvs) * (kv_ld / BKV) + kvb] : a.scale;
