@@ -165,13 +165,14 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* p_ready = bars + 7;
   uint64_t* dq_staged = bars + 8;  // [2] per Q/dO stage: its item's dQ has been read out of it
   uint64_t* ds_ready = bars + 10;
-  uint64_t* ds_consumed = bars + 11;
+  uint64_t* ds_consumed = bars + 11;  // the dS tile free again (FP8: and the dQ chunks staged in it read)
   uint64_t* dq_full = bars + 12;
   uint64_t* dq_drained = bars + 13;
   uint64_t* kv_done = bars + 14;
   uint64_t* q_ready = bars + 15;   // [2] FP8: the stage's Q codes widened (first-half softmax warps)
   uint64_t* k_ready = bars + 17;   // FP8: K's codes widened
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  uint64_t* do_full = bars + 18;   // [2] FP8: a stage's dO tile loaded (qdo_full: its Q tile, lse and D)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* s_lse = reinterpret_cast<float*>(smem + C::LSE_OFF);
   float* s_D = reinterpret_cast<float*>(smem + C::DS_OFF);
@@ -207,12 +208,13 @@ __global__ void __launch_bounds__(512, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&qdo_full[s], 1);
       mbar_init(&qdo_empty[s], 1);
+      mbar_init(&do_full[s], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 256);
     mbar_init(ds_ready, 256);
-    mbar_init(ds_consumed, 1);
+    mbar_init(ds_consumed, F8 ? 4 : 1);  // FP8: lane 0 of each dQ warp
     mbar_init(dq_full, 1);
     mbar_init(dq_drained, 128);
     mbar_init(&dq_staged[0], 4);  // lane 0 of each dQ warp
@@ -255,18 +257,31 @@ __global__ void __launch_bounds__(512, 1)
       for (int i = 0; i < n_items && cur.next(a, kvs); ++i) {
         const int st = i & 1;
         if (!mbar_wait(&qdo_empty[st], ((i >> 1) & 1) ^ 1, w, 40)) break;
-        // the stage's previous item staged its dQ here
-        if (!mbar_wait(&dq_staged[st], ((i >> 1) & 1) ^ 1, w, 39)) break;
         const long long q_row = static_cast<long long>(cur.qs) * a.S + cur.qb * BQ;
-        mbar_arrive_expect_tx(&qdo_full[st], (F8 ? CH : C::TILE) + C::TILE + 2 * BQ * 4);
+        if constexpr (F8) {
+          // Q's codes, lse and D once dK_{i-2} has read the stage's Q tile;
+          // dO once the half of dQ_{i-2} staged in its dO tile has left it
+          mbar_arrive_expect_tx(&qdo_full[st], CH + 2 * BQ * 4);
+          tma_load_2d(smem + C::Q_OFF + st * C::TILE + CH, &tmQ, &qdo_full[st], 0, (int)q_row);
+          bulk_load(s_lse + st * BQ, a.lse2 + q_row, BQ * 4, &qdo_full[st]);
+          bulk_load(s_D + st * BQ, a.Dsum + q_row, BQ * 4, &qdo_full[st]);
+          if (!mbar_wait(&dq_staged[st], ((i >> 1) & 1) ^ 1, w, 39)) break;
+          mbar_arrive_expect_tx(&do_full[st], C::TILE);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          if (!F8) tma_load_2d(smem + C::Q_OFF + st * C::TILE + c * CH, &tmQ, &qdo_full[st], c * 64, (int)q_row);
-          tma_load_2d(smem + C::DO_OFF + st * C::TILE + c * CH, &tmdO, &qdo_full[st], c * 64, (int)q_row);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(smem + C::DO_OFF + st * C::TILE + c * CH, &tmdO, &do_full[st], c * 64, (int)q_row);
+        } else {
+          // the stage's previous item staged its dQ here
+          if (!mbar_wait(&dq_staged[st], ((i >> 1) & 1) ^ 1, w, 39)) break;
+          mbar_arrive_expect_tx(&qdo_full[st], 2 * C::TILE + 2 * BQ * 4);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_2d(smem + C::Q_OFF + st * C::TILE + c * CH, &tmQ, &qdo_full[st], c * 64, (int)q_row);
+            tma_load_2d(smem + C::DO_OFF + st * C::TILE + c * CH, &tmdO, &qdo_full[st], c * 64, (int)q_row);
+          }
+          bulk_load(s_lse + st * BQ, a.lse2 + q_row, BQ * 4, &qdo_full[st]);
+          bulk_load(s_D + st * BQ, a.Dsum + q_row, BQ * 4, &qdo_full[st]);
         }
-        if (F8) tma_load_2d(smem + C::Q_OFF + st * C::TILE + CH, &tmQ, &qdo_full[st], 0, (int)q_row);
-        bulk_load(s_lse + st * BQ, a.lse2 + q_row, BQ * 4, &qdo_full[st]);
-        bulk_load(s_D + st * BQ, a.Dsum + q_row, BQ * 4, &qdo_full[st]);
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------- MMA issuer ----------------
@@ -294,8 +309,12 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
         qk_mma(tmem + C::T_S, sK, sQ(0));
         mma_commit(s_full);
-        qk_mma(tmem + C::T_DP, sV, sdO(0));
-        mma_commit(dp_full);
+        if (F8) ok = mbar_wait(&do_full[0], 0, w, 59);
+        if (ok) {
+          if (F8) tc_fence_after();
+          qk_mma(tmem + C::T_DP, sV, sdO(0));
+          mma_commit(dp_full);
+        }
       }
       for (int i = 0; ok && i < n_items; ++i) {
         const int st = i & 1;
@@ -320,7 +339,7 @@ __global__ void __launch_bounds__(512, 1)
           for (int k = 0; k < BKV / 16; ++k)
             mma_ss(tmem + C::T_DP, sdesc_advance(a1, k * 2048), sdesc_advance(b1, k * 2048), ID_Q, k > 0);
           mma_commit(dq_full);
-          mma_commit(ds_consumed);
+          if (!F8) mma_commit(ds_consumed);
           const uint64_t b0 = sdesc_mnmajor(sQ(st), CH);
 #pragma unroll
           for (int k = 0; k < BQ / 16; ++k)
@@ -339,6 +358,7 @@ __global__ void __launch_bounds__(512, 1)
         // next dP^T once dQ has been drained out of its columns
         if (i + 1 < n_items) {
           if (!mbar_wait(dq_drained, i & 1, w, 46)) break;
+          if (F8 && !mbar_wait(&do_full[st ^ 1], ((i + 1) >> 1) & 1, w, 60)) break;
           tc_fence_after();
           qk_mma(tmem + C::T_DP, sV, sdO(st ^ 1));
           mma_commit(dp_full);
@@ -525,6 +545,7 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
         const int y0 = cur.qs * a.S + cur.qb * BQ + (warp & 3) * 32;
         const uint32_t s_stage = smem_u32(smem) + st * C::TILE + quarter;
+        const uint32_t s_ds = smem_u32(smem + C::DS_TILE_OFF) + (warp & 3) * (BKV * BQ * 2 / 4);
         bool ok = true;
 #pragma unroll 1
         for (int c = 0; ok && c < D / 64; ++c) {
@@ -537,11 +558,16 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int chunk = 2 * c + h;
-            if (chunk == HALF && !mbar_wait_warp(&qdo_empty[st], (i >> 1) & 1, w, 54)) {
+            if (!F8 && chunk == HALF && !mbar_wait_warp(&qdo_empty[st], (i >> 1) & 1, w, 54)) {
               ok = false;
               break;
             }
-            const uint32_t buf = s_stage + (chunk < HALF ? C::DO_OFF : C::Q_OFF) + (chunk % HALF) * 4096;
+            // FP8: the second half in this warp's quarter of the dS tile,
+            // which dQ_i (complete at dq_full) was the last to read, so the
+            // Q tile goes back to the producer as soon as dK_i has read it
+            const uint32_t buf = chunk < HALF ? s_stage + C::DO_OFF + chunk * 4096
+                                 : F8 ? s_ds + (chunk - HALF) * 4096
+                                      : s_stage + C::Q_OFF + (chunk - HALF) * 4096;
 #pragma unroll
             for (int p = 0; p < 8; ++p)
               st_shared_v4(buf + lane * 128 + ((p ^ (lane & 7)) << 4),
@@ -559,8 +585,15 @@ __global__ void __launch_bounds__(512, 1)
         }
         if (!ok) break;
         if (lane == 0) {
-          bulk_wait_read<0>();
-          mbar_arrive(&dq_staged[st]);
+          if constexpr (F8) {  // chunk groups in issue order: the dO tile's first
+            bulk_wait_read<NCH - HALF>();
+            mbar_arrive(&dq_staged[st]);
+            bulk_wait_read<0>();
+            mbar_arrive(ds_consumed);
+          } else {
+            bulk_wait_read<0>();
+            mbar_arrive(&dq_staged[st]);
+          }
         }
         __syncwarp();
       }
