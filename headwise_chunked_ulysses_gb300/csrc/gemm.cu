@@ -36,6 +36,7 @@ struct GemmArgs {
   void* out;
   long long ldo;
   int out_mode;
+  int acc_load;  // fp32 +=: old values read by TMA and the sums stored, instead of reduce-adds
   const float* aux;
   long long ld_aux;
   int* status;
@@ -380,11 +381,14 @@ __global__ void __launch_bounds__(256, 1)
       // ---------------- epilogue: this CTA's 128 rows of the pair tile ----------------
       // fp32 outputs leave through the TMA engine: each warp stages 32 x 32
       // chunks of its rows (128-byte swizzle, two buffers) and stores them, or
-      // adds them atomically into the output (accumulate, split-K partials),
-      // with no read of the old values into the SM
+      // adds them atomically into the output (short-K accumulate, split-K
+      // partials), with no read of the old values into the SM; a long-K
+      // accumulate reads the old chunk by TMA (one ahead, the first while the
+      // tile's accumulator is still being computed), adds and stores
       const int q = warp & 3;
       const int row = q * 32 + lane;
-      const bool tma_out = g.out_mode == kOutF32 || g.out_mode == kOutF32Acc || g.out_mode == kOutF32Red;
+      const bool acc_in = g.out_mode == kOutF32Acc && g.acc_load;
+      const bool tma_out = g.out_mode == kOutF32 || g.out_mode == kOutF32Red || (g.out_mode == kOutF32Acc && !acc_in);
       const bool tma_add = g.out_mode != kOutF32;
       // bf16 = acc + aux: the aux (fp32) chunks come in by TMA, one ahead
       const bool aux_in = g.out_mode == kOutBf16PlusF32;
@@ -394,8 +398,6 @@ __global__ void __launch_bounds__(256, 1)
       int tl = 0;
       for (int t = pair; t < n_tiles; t += n_pairs, ++tl) {
         const int acc = tl & 1;
-        if (!mbar_wait_warp(&tfull[acc], (tl >> 1) & 1, w, 64)) break;
-        tc_fence_after();
         const int m = tile_m0(t) + 128 * static_cast<int>(rank) + row;
         const int n0 = tile_n0(t);
         auto out_col = [&](int c) {
@@ -409,7 +411,13 @@ __global__ void __launch_bounds__(256, 1)
                         out_col(c), m - lane);
           }
         };
-        if (aux_in) load_aux(0, nb);
+        // the tile's first input chunk comes in while its accumulator is
+        // still being computed
+        if (acc_in && lane == 0) bulk_wait_read<0>();  // the stores out of both buffers have been read
+        __syncwarp();
+        if (aux_in || acc_in) load_aux(0, nb);
+        if (!mbar_wait_warp(&tfull[acc], (tl >> 1) & 1, w, 64)) break;
+        tc_fence_after();
         bool ok = true;
 #pragma unroll 1
         for (int c = 0; c < BNP / 32; ++c) {
@@ -430,6 +438,33 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0) {
               if (tma_add) tma_reduce_add_2d(&tmO, buf, oc, m - lane);
               else tma_store_2d(&tmO, buf, oc, m - lane);
+              bulk_commit();
+            }
+            ++nb;
+          } else if (acc_in) {
+            // fp32 +=, the long-K form: the old chunk came in by TMA one chunk
+            // ahead; the sum goes back through the same buffer by a TMA store
+            const uint32_t buf = epi + (nb & 1) * (32 * 32 * 4);
+            if (c + 1 < BNP / 32) {
+              // the next chunk's buffer: its last store has been read
+              if (lane == 0) bulk_wait_read<0>();
+              __syncwarp();
+              load_aux(c + 1, nb + 1);
+            }
+            if (!mbar_wait_warp(&abar[nb & 1], (nb >> 1) & 1, w, 66)) { ok = false; break; }
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+              const uint32_t a = buf + lane * 128 + ((p ^ (lane & 7)) << 4);
+              const uint4 x = ld_shared_v4(a);
+              st_shared_v4(a, __float_as_uint(__uint_as_float(v[4 * p]) + __uint_as_float(x.x)),
+                           __float_as_uint(__uint_as_float(v[4 * p + 1]) + __uint_as_float(x.y)),
+                           __float_as_uint(__uint_as_float(v[4 * p + 2]) + __uint_as_float(x.z)),
+                           __float_as_uint(__uint_as_float(v[4 * p + 3]) + __uint_as_float(x.w)));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmO, buf, oc, m - lane);
               bulk_commit();
             }
             ++nb;
@@ -460,7 +495,7 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
         mbar_arrive_remote(tempty0 + acc * 8);
       }
-      if (tma_out && lane == 0) bulk_wait_all();
+      if ((tma_out || acc_in) && lane == 0) bulk_wait_all();
       __syncwarp();
     }
   }
@@ -545,6 +580,11 @@ cudaError_t launch_gemm(const GemmDesc& d, int* status, cudaStream_t st) {
   copy_map(d.bmap_n, a.use_bmap_n, a.bmap_n);
   copy_map(d.omap_n, a.use_omap_n, a.omap_n);
   a.out = d.out; a.ldo = d.ldo; a.out_mode = d.out_mode;
+  // accumulating outputs of K >= 1536 read the old values and store the sums
+  // (the main loop of a tile is long enough to hide the reads); shorter K
+  // adds through TMA reduce-adds (W_o at K = 1024: 241 against 256 us; dX at
+  // K = 1536: 276 against 302 us)
+  a.acc_load = d.out_mode == kOutF32Acc && d.K >= 1536;
   a.aux = d.aux; a.ld_aux = d.ld_aux;
   a.status = status;
   if (BN == 256 && d.M % 256 == 0 && num_sms() >= 2) {
