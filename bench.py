@@ -340,12 +340,15 @@ def sweep_entries(cases, steps, warmup):
         upipe.profile_enable(True)
         upipe.profile_read()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         e0.record()
-        for _ in range(steps):
+        for i in range(steps):
             _, _, _, stf = fwd(Y=Y, O_saved=O, lse=lse)
             _, _, _, stb = bwd(O, lse, dX=dX, dW_qkv=dWqkv, dW_o=dWo)
+            marks[i].record()
         e1.record()
         torch.cuda.synchronize()
+        per_step = [e0.elapsed_time(marks[0])] + [marks[i - 1].elapsed_time(marks[i]) for i in range(1, steps)]
         clk = clocks.stop()
         prof = upipe.profile_read()
         upipe.profile_enable(False)
@@ -359,7 +362,8 @@ def sweep_entries(cases, steps, warmup):
         yield {
             "sweep": name, "S": sh.S, "U": sh.U, "C": sh.C, "H": sh.H, "G": sh.G, "d_model": sh.d_model,
             "schedule": "gqa_out_of_order" if sched else "in_order", "steps": steps, "warmup": warmup,
-            "ms_per_step": ms, "tokens_per_s": sh.S / (ms / 1e3), "tflops": tf,
+            "ms_per_step": ms, "ms_per_step_min_max": [min(per_step), max(per_step)],
+            "tokens_per_s": sh.S / (ms / 1e3), "tflops": tf,
             "frac_of_bf16_peak": tf / pk["bf16_tflops"],
             "frac_of_bf16_peak_sustained": tf / pk["bf16_tflops_sustained"],
             "attn_bwd_tflops": bwd_tf,
@@ -497,11 +501,14 @@ def main():
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     e0.record(stream)
-    for _ in range(args.steps):
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
         stf, stb = step()
+        marks[i].record(stream)
     e1.record(stream)
     barrier()
     elapsed_ms = e0.elapsed_time(e1)
+    per_step = [e0.elapsed_time(marks[0])] + [marks[i - 1].elapsed_time(marks[i]) for i in range(1, args.steps)]
     prof = upipe.profile_read()
     upipe.profile_enable(False)
     clk = clocks.stop()
@@ -664,7 +671,8 @@ def main():
                          f"({dt:.1f} s), extrapolated to S={sh.S} by the model-FLOP ratio"}
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_min_max": [min(per_step), max(per_step)],
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(args, sh),
         "tflops": tflops, "frac_of_bf16_peak": tflops / peak_tf,
         "frac_of_bf16_peak_sustained": tflops / peak_sus,
