@@ -42,6 +42,18 @@ struct GemmArgs {
   int* status;
 };
 
+// The K-block gather maps go to shared memory before the main loop: the
+// producer thread reads one entry of each per K block, right after waiting
+// for a free ring stage, and a dynamically indexed kernel parameter is a
+// constant-cache load that can miss (a miss there delays every refill).
+__device__ __forceinline__ void stage_k_maps(const GemmArgs& g, uint16_t* kmap, int lane) {
+  const int n = g.K / BK;
+  if (g.use_amap_k)
+    for (int i = lane; i < n; i += 32) kmap[i] = g.amap_k[i];
+  if (g.use_bmap_k)
+    for (int i = lane; i < n; i += 32) kmap[kMaxMap + i] = g.bmap_k[i];
+}
+
 template <int BN>
 struct Cfg {
   static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
@@ -50,7 +62,8 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int SMEM = BAR_OFF + 256;
+  static constexpr int MAP_OFF = BAR_OFF + 256;  // K-block maps of A and B: 2 x kMaxMap uint16
+  static constexpr int SMEM = MAP_OFF + 2 * kMaxMap * 2;
 };
 
 __device__ __forceinline__ void store_tile_chunk(const GemmArgs& g, int m, int oc, const uint32_t (&v)[32]) {
@@ -132,33 +145,39 @@ __global__ void __launch_bounds__(256, 1)
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
   }
+  uint16_t* kmap = reinterpret_cast<uint16_t*>(smem + C::MAP_OFF);
+  if (warp == 3) stage_k_maps(g, kmap, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n_tiles = g.m_tiles * g.n_tiles * g.split_k;
-  const int kblocks = g.K / BK / g.split_k;  // k blocks per tile
-  // tile t: split ks = t / (m_tiles*n_tiles), then m-major, n fastest
+  const int kb_all = g.K / BK;
+  // tile t: split ks = t / (m_tiles*n_tiles), then m-major, n fastest; split
+  // ks covers K blocks [ks*kb_all/split_k, (ks+1)*kb_all/split_k)
   auto tile_m0 = [&](int t) { return ((t % (g.m_tiles * g.n_tiles)) / g.n_tiles) * BM; };
   auto tile_n0 = [&](int t) { return (t % g.n_tiles) * BN; };
-  auto tile_kb0 = [&](int t) { return (t / (g.m_tiles * g.n_tiles)) * kblocks; };
+  auto tile_kb0 = [&](int t) { return (t / (g.m_tiles * g.n_tiles)) * kb_all / g.split_k; };
+  auto tile_kbs = [&](int t) { return tile_kb0(t + g.m_tiles * g.n_tiles) - tile_kb0(t); };
 
   if (aligned) {
     if (warp == 0 && lane == 0) {
       // ---------------- TMA producer ----------------
-      int it = 0;
+      int s = 0;        // ring stage
+      uint32_t ph = 0;  // its phase parity
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
-        const int m0 = tile_m0(t), n0 = tile_n0(t), kb0 = tile_kb0(t);
-        for (int kb = kb0; kb < kb0 + kblocks; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
+        const int m0 = tile_m0(t), n0 = tile_n0(t), kb0 = tile_kb0(t), kb1 = kb0 + tile_kbs(t);
+        int nc[BN / 64];  // the tile's B columns, fixed over its K loop
+#pragma unroll
+        for (int i = 0; i < BN / 64; ++i) nc[i] = (g.use_bmap_n ? g.bmap_n[n0 / 64 + i] : n0 / 64 + i) * 64;
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1, w, 1)) { ok = false; break; }
           uint8_t* sa = smem + s * C::STAGE_BYTES;
           uint8_t* sb = sa + C::A_BYTES;
           mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-          const int ka = (g.use_amap_k ? g.amap_k[kb] : kb) * BK;
-          const int kbb = (g.use_bmap_k ? g.bmap_k[kb] : kb) * BK;
+          const int ka = (g.use_amap_k ? kmap[kb] : kb) * BK;
+          const int kbb = (g.use_bmap_k ? kmap[kMaxMap + kb] : kb) * BK;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             if (A_MN) tma_load_2d(sa + i * BOX_BYTES, &tmA, &full[s], m0 + 64 * i, ka);
@@ -166,26 +185,29 @@ __global__ void __launch_bounds__(256, 1)
           }
 #pragma unroll
           for (int i = 0; i < BN / 64; ++i) {
-            const int nb = n0 / 64 + i;
-            const int nc = (g.use_bmap_n ? g.bmap_n[nb] : nb) * 64;
-            if (B_MN) tma_load_2d(sb + i * BOX_BYTES, &tmB, &full[s], nc, kbb);
-            else      tma_load_2d(sb + i * BOX_BYTES, &tmB, &full[s], kbb, nc);
+            if (B_MN) tma_load_2d(sb + i * BOX_BYTES, &tmB, &full[s], nc[i], kbb);
+            else      tma_load_2d(sb + i * BOX_BYTES, &tmB, &full[s], kbb, nc[i]);
+          }
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
           }
         }
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------- MMA issuer ----------------
       constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
-      int it = 0, tl = 0;
+      int s = 0, tl = 0;
+      uint32_t ph = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++tl) {
         const int acc = tl & 1;
         if (!mbar_wait(&tempty[acc], ((tl >> 1) & 1) ^ 1, w, 2)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * BN;
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % STAGES;
-          if (!mbar_wait(&full[s], (it / STAGES) & 1, w, 3)) { ok = false; break; }
+        const int kblocks = tile_kbs(t);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[s], ph, w, 3)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * C::STAGE_BYTES);
           const uint32_t sb = sa + C::A_BYTES;
@@ -198,6 +220,10 @@ __global__ void __launch_bounds__(256, 1)
             mma_ss(d_tmem, ad, bd, IDESC, (kb | k) != 0);
           }
           mma_commit(&empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
         }
         if (ok) mma_commit(&tfull[acc]);
       }
@@ -257,7 +283,8 @@ struct Cfg2 {
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;  // fp32 output staging: 4 warps x 2 x (32 x 32)
   static constexpr int EPI_BYTES = 4 * 2 * 32 * 32 * 4;
   static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
-  static constexpr int SMEM = BAR_OFF + 256;
+  static constexpr int MAP_OFF = BAR_OFF + 256;  // K-block maps of A and B: 2 x kMaxMap uint16
+  static constexpr int SMEM = MAP_OFF + 2 * kMaxMap * 2;
 };
 
 template <bool A_MN, bool B_MN>
@@ -303,6 +330,8 @@ __global__ void __launch_bounds__(256, 1)
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
   }
+  uint16_t* kmap = reinterpret_cast<uint16_t*>(smem + C::MAP_OFF);
+  if (warp == 3) stage_k_maps(g, kmap, lane);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // both CTAs' barriers are initialised before any remote use
@@ -310,58 +339,66 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tmem = *tmem_slot;
   const int pair = static_cast<int>(blockIdx.x) >> 1, n_pairs = static_cast<int>(gridDim.x) >> 1;
   const int n_tiles = g.m_tiles * g.n_tiles * g.split_k;  // m_tiles counts 256-row tiles here
-  const int kblocks = g.K / BK / g.split_k;
+  const int kb_all = g.K / BK;
   auto tile_m0 = [&](int t) { return ((t % (g.m_tiles * g.n_tiles)) / g.n_tiles) * 256; };
   auto tile_n0 = [&](int t) { return (t % g.n_tiles) * BNP; };
-  auto tile_kb0 = [&](int t) { return (t / (g.m_tiles * g.n_tiles)) * kblocks; };
+  auto tile_kb0 = [&](int t) { return (t / (g.m_tiles * g.n_tiles)) * kb_all / g.split_k; };
+  auto tile_kbs = [&](int t) { return tile_kb0(t + g.m_tiles * g.n_tiles) - tile_kb0(t); };
   const uint32_t full0 = mapa_shared(smem_u32(full), 0);     // CTA 0's full[0]
   const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0); // CTA 0's tempty[0]
 
   if (aligned) {
     if (warp == 0 && lane == 0) {
       // ---------------- TMA producer (both CTAs) ----------------
-      int it = 0;
+      int s = 0;        // ring stage
+      uint32_t ph = 0;  // its phase parity
       bool ok = true;
       for (int t = pair; ok && t < n_tiles; t += n_pairs) {
         const int m0 = tile_m0(t) + 128 * static_cast<int>(rank), n0 = tile_n0(t) + 128 * static_cast<int>(rank);
-        const int kb0 = tile_kb0(t);
-        for (int kb = kb0; kb < kb0 + kblocks; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
+        const int kb0 = tile_kb0(t), kb1 = kb0 + tile_kbs(t);
+        // the tile's B columns are fixed over its K loop
+        const int nc0 = (g.use_bmap_n ? g.bmap_n[n0 / 64] : n0 / 64) * 64;
+        const int nc1 = (g.use_bmap_n ? g.bmap_n[n0 / 64 + 1] : n0 / 64 + 1) * 64;
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1, w, 61)) { ok = false; break; }
           uint8_t* sa = smem + s * C::STAGE_BYTES;
           uint8_t* sb = sa + C::A_BYTES;
           const uint32_t fb = full0 + s * 8;
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
-          const int ka = (g.use_amap_k ? g.amap_k[kb] : kb) * BK;
-          const int kbb = (g.use_bmap_k ? g.bmap_k[kb] : kb) * BK;
+          const int ka = (g.use_amap_k ? kmap[kb] : kb) * BK;
+          const int kbb = (g.use_bmap_k ? kmap[kMaxMap + kb] : kb) * BK;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             if (A_MN) tma_load_2d_pair(sa + i * BOX_BYTES, &tmA, fb, m0 + 64 * i, ka);
             else      tma_load_2d_pair(sa + i * BOX_BYTES, &tmA, fb, ka, m0 + 64 * i);
           }
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int nb = n0 / 64 + i;
-            const int nc = (g.use_bmap_n ? g.bmap_n[nb] : nb) * 64;
-            if (B_MN) tma_load_2d_pair(sb + i * BOX_BYTES, &tmB, fb, nc, kbb);
-            else      tma_load_2d_pair(sb + i * BOX_BYTES, &tmB, fb, kbb, nc);
+          if (B_MN) {
+            tma_load_2d_pair(sb, &tmB, fb, nc0, kbb);
+            tma_load_2d_pair(sb + BOX_BYTES, &tmB, fb, nc1, kbb);
+          } else {
+            tma_load_2d_pair(sb, &tmB, fb, kbb, nc0);
+            tma_load_2d_pair(sb + BOX_BYTES, &tmB, fb, kbb, nc1);
+          }
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
           }
         }
       }
     } else if (warp == 1 && lane == 0 && rank == 0) {
       // ---------------- MMA issuer (CTA 0 only) ----------------
       constexpr uint32_t IDESC = idesc_bf16(256, BNP, A_MN, B_MN);
-      int it = 0, tl = 0;
+      int s = 0, tl = 0;
+      uint32_t ph = 0;
       bool ok = true;
       for (int t = pair; ok && t < n_tiles; t += n_pairs, ++tl) {
         const int acc = tl & 1;
         if (!mbar_wait(&tempty[acc], ((tl >> 1) & 1) ^ 1, w, 62)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * BNP;
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % STAGES;
-          if (!mbar_wait(&full[s], (it / STAGES) & 1, w, 63)) { ok = false; break; }
+        const int kblocks = tile_kbs(t);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[s], ph, w, 63)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * C::STAGE_BYTES);
           const uint32_t sb = sa + C::A_BYTES;
@@ -374,6 +411,10 @@ __global__ void __launch_bounds__(256, 1)
             mma_ss_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0);
           }
           mma_commit_pair(&empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
         }
         if (ok) mma_commit_pair(&tfull[acc]);
       }
@@ -564,7 +605,12 @@ void copy_map(const BlockMap& m, int& use, uint16_t* dst) {
 
 cudaError_t launch_gemm(const GemmDesc& d, int* status, cudaStream_t st) {
   if (d.M % 64 || d.K % BK || d.N % 64 || d.M <= 0 || d.N <= 0 || d.K <= 0) return cudaErrorInvalidValue;
-  if (d.split_k < 1 || (d.K / BK) % d.split_k || (d.split_k > 1 && d.out_mode != kOutF32Red))
+  if (d.split_k < 1 || d.K / BK < d.split_k || (d.split_k > 1 && d.out_mode != kOutF32Red))
+    return cudaErrorInvalidValue;
+  // a gather map names every 64-wide block of its dimension
+  auto map_ok = [](const BlockMap& m, int blocks) { return m.n == 0 || (m.n == blocks && blocks <= kMaxMap); };
+  if (!map_ok(d.amap_k, d.K / BK) || !map_ok(d.bmap_k, d.K / BK) || !map_ok(d.bmap_n, d.N / 64) ||
+      !map_ok(d.omap_n, d.N / 64))
     return cudaErrorInvalidValue;
   const int BN = (d.N % 256 == 0) ? 256 : (d.N % 128 == 0 ? 128 : 64);
   CUtensorMap ta, tb;

@@ -351,20 +351,24 @@ bool all_stages_fp8(const Plan& p, const uint8_t* fp8_heads) {
 int choose_split_k(const GemmDesc& g) {
   const int bn = (g.N % 256 == 0) ? 256 : (g.N % 128 == 0 ? 128 : 64);
   const bool pair = bn == 256 && g.M % 256 == 0 && num_sms() >= 2;
-  const long long tiles = pair ? static_cast<long long>(g.M / 256) * (g.N / 256)
+  const long long tiles = pair ? static_cast<long long>(g.M / 256) * (g.N / bn)
                                : static_cast<long long>((g.M + 127) / 128) * (g.N / bn);
   const long long slots = pair ? num_sms() / 2 : num_sms();
   const int kb = g.K / 64;
+  // a split's K range is kb/s blocks, rounded either way; the estimated time
+  // is the number of rounds of work units times the longest range, and a
+  // larger split is taken only when it is at least 2 % faster (its partial
+  // sums add more fp32 traffic)
   int best = 1;
-  double best_fill = -1.0;
+  double best_time = 0.0;
   for (int s = 1; s <= 8; ++s) {
-    if (kb % s || kb / s < 8) continue;
+    if (kb / s < 8) break;
     if (s > 1 && static_cast<long long>(s) * g.M * g.N * 4 > (1LL << 28)) break;
     const long long units = tiles * s, rounds = (units + slots - 1) / slots;
-    const double fill = static_cast<double>(units) / static_cast<double>(rounds * slots);
-    if (fill > best_fill + 0.02) {
+    const double time = static_cast<double>(rounds) * static_cast<double>((kb + s - 1) / s);
+    if (s == 1 || time < 0.98 * best_time) {
       best = s;
-      best_fill = fill;
+      best_time = time;
     }
   }
   return best;

@@ -38,7 +38,7 @@ struct GemmDesc {
   BlockMap amap_k, bmap_k, bmap_n, omap_n;
   void* out = nullptr; long long ldo = 0; int out_mode = kOutF32;
   const float* aux = nullptr; long long ld_aux = 0;
-  int split_k = 1;  // > 1 only with kOutF32Red: K is cut into split_k equal ranges
+  int split_k = 1;  // > 1 only with kOutF32Red: K is cut into split_k ranges of K/64/split_k blocks, rounded either way
 };
 
 // Epilogues of the attention forward: one launch over all keys (plain), or

@@ -3,9 +3,9 @@
 * the Ulysses exchange (seq->head, head->seq): bit-exact against the oracle's
   all-to-all of C virtual ranks;
 * the tensor-core contraction in all four operand layouts and four output
-  modes (incl. split-K with atomic partial sums), on one SM and on CTA pairs
-  (M and N multiples of 256): against an fp64 product of the same bf16
-  operands;
+  modes (incl. split-K with atomic partial sums over K ranges of equal and
+  unequal length), on one SM and on CTA pairs (M and N multiples of 256):
+  against an fp64 product of the same bf16 operands;
 * causal GQA attention forward and backward: against the oracle's attention
   core (fp64), per head; dK, dV summed over the query heads of each group.
 """
@@ -66,7 +66,12 @@ def test_exchange_is_bit_exact(up, S, n_heads, d, C, pad):
 @pytest.mark.parametrize("M,N,K", [(256, 384, 320), (128, 512, 128), (384, 64, 192), (256, 256, 1024),
                                    (128, 256, 8192), (512, 512, 512), (768, 1280, 576), (256, 256, 16384),
                                    # M a multiple of 64 only: a last row tile of 64 rows
-                                   (64, 256, 192), (192, 384, 320), (320, 1536, 8192)])
+                                   (64, 256, 192), (192, 384, 320), (320, 1536, 8192),
+                                   # split-K ranges of unequal length (on 152 SMs: 2 splits over 21
+                                   # K blocks on one SM; 8 and 7 splits over 65 on CTA pairs)
+                                   (128, 768, 1344), (256, 512, 4160), (1280, 512, 4160),
+                                   # CTA pairs on 152 SMs: 80 tiles, a second round of 4
+                                   (5120, 1024, 128)])
 @pytest.mark.parametrize("a_trans,b_trans", [(0, 0), (0, 1), (1, 0), (1, 1)])
 def test_gemm_layouts_and_modes(up, M, N, K, a_trans, b_trans):
     import torch
