@@ -12,7 +12,11 @@
 // accumulator (tcgen05.ld) and write the epilogue, so the epilogue of tile t
 // overlaps the main loop of tile t+1.  Every box coordinate passes through an
 // optional 64-block gather map, which is how the non-contiguous head sets of
-// the out-of-order schedule are read without copies.
+// the out-of-order schedule are read without copies; the K maps are copied
+// into shared memory before the main loop, so per K block the producer only
+// waits for a free stage, reads two map entries and issues its loads.  Split-K
+// (few output tiles, long K) cuts K into ranges of about K/64/split_k blocks
+// whose fp32 partial sums the TMA engine adds into the output.
 #include <algorithm>
 
 #include "ptx.cuh"
